@@ -1,0 +1,385 @@
+"""Benchmark of the selective-SSM serving step on GB300.
+
+One step = the whole hot path over one batch of the long-context mixed
+workload (8 fresh prefills of 65536 tokens plus 384 single-token decodes,
+chunk 256, H=128, P=64, N=128, G=8, bf16 tokens, fp32 state cache of 16384
+slots): host chunk metadata, its copy to the device, ssd_prefill_varlen,
+ssm_decode_update.  Inputs are seeded synthetic tensors of that shape; the
+inputs (8.6 GB of x alone) are larger than the 129 MB L2, so no flush is
+needed between steps.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead, on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "SSD prefill tokens/s/layer and decode state-updates/s; % HBM roofline on 1 GB300"
+UNIT = "tokens/s/layer"
+WORKLOAD = dict(workload="long-context mixed batch: 8 x 65536-token prefills + 384 single-token decodes",
+                num_prefills=8, prefill_len=65536, num_decodes=384, chunk_size=256, nheads=128,
+                headdim=64, dstate=128, ngroups=8, cache_slots=16384, token_dtype="bf16",
+                state_dtype="fp32", l2="inputs larger than L2 (no flush)")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------- byte counts --
+
+def prefill_bytes(T, K, H, P, N, G, elt, init_reads=0):
+    """Algorithmic HBM bytes of one prefill call: x in, y out, dt, B, C per
+    token; one fp32 state store per chunk; one state load per initial state."""
+    per_tok = 2 * H * P * elt + H * elt + 2 * G * N * elt
+    return T * per_tok + (K + init_reads) * H * P * N * 4
+
+
+def decode_bytes(live, tpr, writes, H, P, N, G, elt):
+    """One state load per live request, one state store per written column,
+    plus the token tensors of the live rows."""
+    per_tok = 2 * H * P * elt + H * elt + 2 * G * N * elt
+    return (live + writes) * H * P * N * 4 + live * tpr * per_tok
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [v.strip() for v in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- GPU arm -----
+
+class Step:
+    """Holds one rank's device-resident workload and runs the step."""
+
+    def __init__(self, dev):
+        import selective_state_space_mamba2_gb300 as ssd
+        from selective_state_space_mamba2_gb300 import workloads as W
+        self.ssd = ssd
+        self.dev = dev
+        self.pre, self.dec = W.long_mixed(dev)
+        p = self.pre
+        self.H, self.P = p["x"].shape[1], p["x"].shape[2]
+        self.G, self.N = p["B"].shape[1], p["B"].shape[2]
+        self.y = torch.empty_like(p["x"])
+        self.yd = torch.empty_like(self.dec["x"])
+        self.cu_dev = p["cu_seqlens"].to(dev)
+        self.si_dev = self.dec["state_indices"].to(dev)
+        self.meta = self.metadata()
+        self.K = len(self.meta["seq_idx"])
+        m = self.device_meta(self.meta)
+        a = ssd.prefill_args(p["x"], p["dt"], p["A"], p["B"], p["C"], self.cu_dev, m["cu_chunk_seqlens"],
+                             m["seq_idx"], m["last_chunk_indices"], self.y, m["init_slot"], m["chunk_slot"],
+                             p["cache"], p["D"], p["dt_bias"], chunk_size=p["chunk_size"])
+        self.workspace = torch.empty(max(ssd.ssd_prefill_workspace_size(a), 1), dtype=torch.uint8, device=dev)
+        self.prefill_kernels = ssd.ssd_prefill_kernel_count(a)
+        self.stream = torch.cuda.current_stream()
+
+    def metadata(self):
+        p = self.pre
+        return self.ssd.ssd_chunk_metadata(p["cu_seqlens"], p["chunk_size"], p["num_computed"], p["has_init"],
+                                           block_table=p["block_table"], null_block_id=p["null_block_id"])
+
+    def device_meta(self, meta):
+        return {k: torch.from_numpy(v).to(self.dev, non_blocking=True) for k, v in meta.items()}
+
+    def run(self, ev=None, host=None):
+        """One step.  ev: optional (start, mid, end) CUDA events around the
+        prefill and decode calls.  host: pinned host buffers for the e2e leg."""
+        p, d = self.pre, self.dec
+        if host is not None:  # end to end: this step's inputs come from host memory
+            for name in ("x", "dt", "B", "C"):
+                p[name].copy_(host["p_" + name], non_blocking=True)
+                d[name].copy_(host["d_" + name], non_blocking=True)
+        meta = self.metadata()
+        m = self.device_meta(meta)
+        if ev is not None:
+            ev[0].record()
+        self.ssd.ssd_prefill_varlen(p["x"], p["dt"], p["A"], p["B"], p["C"], self.cu_dev, m["cu_chunk_seqlens"],
+                                    m["seq_idx"], m["last_chunk_indices"], out=self.y, init_slot=m["init_slot"],
+                                    chunk_slot=m["chunk_slot"], state_cache=p["cache"], D=p["D"],
+                                    dt_bias=p["dt_bias"], null_block_id=p["null_block_id"],
+                                    chunk_size=p["chunk_size"], workspace=self.workspace)
+        if ev is not None:
+            ev[1].record()
+        self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
+                                   out=self.yd, D=d["D"], dt_bias=d["dt_bias"], null_block_id=d["null_block_id"])
+        if ev is not None:
+            ev[2].record()
+        if host is not None:
+            host["y"].copy_(self.y, non_blocking=True)
+            host["yd"].copy_(self.yd, non_blocking=True)
+
+    def host_buffers(self):
+        p, d = self.pre, self.dec
+        h = {}
+        for name in ("x", "dt", "B", "C"):
+            h["p_" + name] = torch.empty(p[name].shape, dtype=p[name].dtype, pin_memory=True)
+            h["p_" + name].copy_(p[name])
+            h["d_" + name] = torch.empty(d[name].shape, dtype=d[name].dtype, pin_memory=True)
+            h["d_" + name].copy_(d[name])
+        h["y"] = torch.empty(self.y.shape, dtype=self.y.dtype, pin_memory=True)
+        h["yd"] = torch.empty(self.yd.shape, dtype=self.yd.dtype, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for k, v in h.items() if k[:2] in ("p_", "d_"))
+        meta_bytes = sum(v.nbytes for v in self.meta.values())
+        d2h = h["y"].numel() * 2 + h["yd"].numel() * 2
+        return h, h2d + meta_bytes, d2h
+
+
+def _barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(v, dist_on, dev):
+    if not dist_on:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def gpu_arm(args, rank, world, dist_on):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    import selective_state_space_mamba2_gb300 as ssd
+    ssd.build()
+    st = Step(dev)
+    H, P, N, G = st.H, st.P, st.N, st.G
+    T = int(st.pre["cu_seqlens"][-1])
+    R = st.dec["live"]
+    pre_bytes = prefill_bytes(T, st.K, H, P, N, G, 2)
+    dec_bytes = decode_bytes(R, 1, R, H, P, N, G, 2)
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        _barrier(dist_on)
+        torch.cuda.synchronize()
+        t0.record()
+        for i in range(args.steps):
+            st.run(ev=evs[i])
+        t1.record()
+        torch.cuda.synchronize()
+        _barrier(dist_on)
+    elapsed_ms = _max_over_ranks(t0.elapsed_time(t1), dist_on, dev)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+
+    # end to end: inputs from pinned host memory, y back to host, every step
+    host, h2d, d2h = st.host_buffers()
+    st.run(host=host)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    _barrier(dist_on)
+    e0.record()
+    for _ in range(args.steps):
+        st.run(host=host)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), dist_on, dev)
+
+    if rank != 0:
+        return None
+    ms_step = elapsed_ms / args.steps
+    units = (T + R) * world
+    hbm, peak_kind = _peaks()
+    pre_mean = statistics.mean(pre_ms)
+    achieved = pre_bytes / (pre_mean * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": units / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded randn tokens, -exp(U(0,2)) A, U(-4,-1) dt_bias)",
+        "config": dict(WORKLOAD, parallelism="dp%d (independent replicas)" % world),
+        "prefill": {"tokens_per_s_per_layer": T / (pre_mean * 1e-3), "ms": pre_mean,
+                    "algorithmic_bytes": pre_bytes,
+                    "hbm_frac": achieved / hbm},
+        "decode": {"state_updates_per_s": R / (statistics.mean(dec_ms) * 1e-3), "ms": statistics.mean(dec_ms),
+                   "algorithmic_bytes": dec_bytes,
+                   "hbm_frac": dec_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9 / hbm},
+        "roofline": {"kernel": "ssd_prefill_varlen (%d kernels)" % st.prefill_kernels, "bound": "hbm",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": peak_kind, "traffic": None,
+                     "units": "prefill algorithmic bytes per call / mean call time (CUDA events)"},
+        "clocks": clk.summary(),
+        "e2e": {"value": units / (e2e_ms / args.steps * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": (st.prefill_kernels + 1) * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+# -------------------------------------------------------------- CPU arm -----
+
+def _oracle_sample(tokens, seed=4):
+    """A prefix of one prefill sequence of the same workload (all 128 heads),
+    generated on the CPU with the workload's distributions."""
+    from selective_state_space_mamba2_gb300 import workloads as W
+    c = W.prefill_case(seed, [tokens], [0], WORKLOAD["nheads"], WORKLOAD["headdim"], WORKLOAD["dstate"],
+                       WORKLOAD["ngroups"], WORKLOAD["chunk_size"], device="cpu", num_slots=2, mode="default")
+    return c
+
+
+def _time_oracle(c, threads):
+    import oracle
+    T = c["x"].shape[0]
+    cc = np.arange(0, T + 1, WORKLOAD["chunk_size"], dtype=np.int32)
+    if cc[-1] != T:
+        cc = np.append(cc, T).astype(np.int32)
+    args = [c[k].double().numpy() for k in ("x", "dt", "A", "B", "C")]
+    t = time.perf_counter()
+    oracle.ssd_prefill(args[0], args[1], args[2], args[3], args[4], [0, T], cc, D=c["D"], dt_bias=c["dt_bias"],
+                       nthreads=threads)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(target_s=15.0):
+    import oracle
+    threads = oracle.default_threads()
+    probe = 256
+    dt = _time_oracle(_oracle_sample(probe), threads)
+    tokens = int(max(probe, min(65536, probe * target_s / max(dt, 1e-3))))
+    tokens = max(256, (tokens // 256) * 256)
+    dt = _time_oracle(_oracle_sample(tokens), threads)
+    return {"value": tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "first %d tokens of one 65536-token prefill, all 128 heads, fp64 sequential recurrence "
+                      "(%.1f s)" % (tokens, dt)}
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    probe = 256
+    dt = _time_oracle(_oracle_sample(probe), threads)
+    budget = 150.0 / max(args.steps + args.warmup, 1)  # whole run within a few minutes
+    tokens = max(256, (int(probe * budget / max(dt, 1e-3)) // 256) * 256)
+    tokens = min(tokens, 65536)
+    c = _oracle_sample(tokens)
+    for _ in range(args.warmup):
+        _time_oracle(c, threads)
+    times = [_time_oracle(c, threads) for _ in range(args.steps)]
+    v = tokens / statistics.mean(times)
+    return {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": statistics.mean(times) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(WORKLOAD, parallelism="host cores"), "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "first %d tokens of one 65536-token prefill, all 128 heads" % tokens},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist_on = world > 1
+    if args.impl == "reference":
+        line = reference_arm(args, rank)
+    else:
+        args.warmup = max(args.warmup, 3)  # timing rule: at least 3 warm-up steps
+        if dist_on:
+            torch.distributed.init_process_group("nccl")
+        line = gpu_arm(args, rank, world, dist_on)
+        if dist_on:
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,261 @@
+/*
+ * ssd.h -- C ABI of the GB300 selective-SSM (Mamba2 SSD) serving library.
+ *
+ * Three calls make up the serving hot path of a Mamba2 layer's state-space
+ * part:
+ *
+ *   ssd_chunk_metadata  host:   varlen chunk metadata and slot routing
+ *   ssd_prefill_varlen  device: chunked SSD prefill scan over packed sequences
+ *   ssm_decode_update   device: single/speculative-token decode state update
+ *
+ * The recurrence (per head h, group g = h / (nheads / ngroups)):
+ *   delta_t = clamp(softplus(dt[t,h] + dt_bias[h]), dt_min, dt_max)
+ *   s_t     = exp(delta_t * A[h]) * s_{t-1} + delta_t * x[t,h,:] (outer) B[t,g,:]
+ *   y[t,h]  = s_t . C[t,g,:] + D[h] * x[t,h,:]
+ * with s a [headdim, dstate] fp32 state.  This is the selective SSM (S6)
+ * whose Delta, B and C depend on the input, as summarised on
+ * "[vLLM] Mamba (SSM): 선형 시간 복잡도 시퀀스 모델링", section
+ * "논문 핵심 내용"; the argument set (dt_bias, dt_softplus, dt_limit, D,
+ * grouped B/C, state dtype) is that of the varlen chunk-scan call on
+ * "[vllm] vLLM Mamba2 SSD 커널 웜업", section "mamba_mixer2.py 변경 사항 (핵심)".
+ *
+ * Conventions shared by every call
+ *   - All tensors are dense and row-major (last index fastest).
+ *   - "device" pointers are CUDA global memory of the current device;
+ *     "host" pointers are ordinary CPU memory.  The caller owns every buffer.
+ *   - Device calls are asynchronous on the given stream.  They launch CUDA
+ *     kernels and return; they never synchronise, never allocate and keep no
+ *     state between calls.
+ *   - Host-side argument checks return a status synchronously and launch
+ *     nothing.  Problems only visible on the device (a slot id outside
+ *     [0, num_slots), metadata that contradicts cu_seqlens) set bits in the
+ *     optional device word *err_word (atomic OR; the caller zeroes it and
+ *     reads it after synchronising); the offending access is skipped.
+ *   - A slot id equal to null_block_id is never read or written, even when
+ *     null_block_id is itself a valid index such as 0.
+ *   - State slots of different sequences / requests must not alias.  Within
+ *     one sequence the initial-state slot may equal a chunk's output slot; the
+ *     initial state is read before any state of that sequence is written.
+ */
+#ifndef SSD_GB300_SSD_H
+#define SSD_GB300_SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same type); NULL is the legacy default stream. */
+typedef struct CUstream_st *ssd_stream_t;
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1, /* a size, pointer, alignment or index argument is invalid */
+    SSD_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. z != NULL) */
+    SSD_ERR_WORKSPACE = 3,   /* workspace (or max_chunks) too small */
+    SSD_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} ssd_status_t;
+
+/* element type of x, dt, B, C and y; A, D, dt_bias and the state are fp32 */
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype_t;
+
+/* bits OR-ed into *err_word by the kernels */
+#define SSD_DEVERR_SLOT 0x1u     /* a slot id not null and outside [0, num_slots) */
+#define SSD_DEVERR_METADATA 0x2u /* chunk metadata inconsistent with cu_seqlens */
+#define SSD_DEVERR_COLUMN 0x4u   /* num_accepted_tokens outside [0, state_indices_cols) */
+#define SSD_DEVERR_TIMEOUT 0x8u  /* a bounded device-side wait gave up */
+
+/* Human-readable name of a status code (static string). */
+SSD_API const char *ssd_status_string(ssd_status_t status);
+
+/* ABI version of this header; bumped on any incompatible change. */
+#define SSD_ABI_VERSION 1
+SSD_API int32_t ssd_abi_version(void);
+
+/* ------------------------------------------------------------------------ *
+ * Chunk metadata (host)
+ *
+ * Follows "[vLLM] Mamba (SSM): 선형 시간 복잡도 시퀀스 모델링", section
+ * "청크 메타데이터 계산": every chunk holds tokens of a single sequence, and a
+ * chunk ends at every absolute multiple of chunk_size so the state can be
+ * stored every chunk_size tokens (prefix caching).  A sequence whose
+ * num_computed_tokens is not a multiple of chunk_size first closes the
+ * unaligned remainder of its previous chunk, then continues with full chunks
+ * and a partial tail.  Slot routing follows "MetadataBuilder 초기화"
+ * ("all" cache mode keeps one state per block; the default mode keeps one per
+ * request).
+ * ------------------------------------------------------------------------ */
+
+/* Upper bound on the number of chunks: min(T, 2*S + ceil(T/chunk_size)).
+ * Returns -1 for invalid arguments. */
+SSD_API int32_t ssd_max_chunks(int32_t num_seqs, int32_t total_tokens, int32_t chunk_size);
+
+/*
+ * All pointers are HOST memory.  Inputs:
+ *   cu_seqlens          [S+1]  cu_seqlens[0] == 0, non-decreasing; sequence r owns
+ *                              packed tokens [cu_seqlens[r], cu_seqlens[r+1]).
+ *   num_computed_tokens [S]    tokens of r already processed earlier (>= 0), or
+ *                              NULL for all zero.  Sets the absolute position of
+ *                              r's first new token and so the chunk alignment.
+ *   has_initial_states  [S]    nonzero: r resumes from a stored state; NULL = none.
+ *   block_table         [S, block_table_stride] "all" mode: slot of block j of r
+ *                              (block j covers absolute positions
+ *                              [j*chunk_size, (j+1)*chunk_size)); NULL otherwise.
+ *                              block_table_cols = valid columns per row.
+ *   state_indices       [S]    default mode (block_table == NULL): r's single slot;
+ *                              may be NULL.
+ *   null_block_id              slot id meaning "no slot".
+ * Outputs (capacity max_chunks, which must be >= the number of chunks K):
+ *   cu_chunk_seqlens    [K+1]  chunk k owns tokens [cu_chunk_seqlens[k], cu_chunk_seqlens[k+1]).
+ *   seq_idx             [K]    sequence of chunk k.
+ *   last_chunk_indices  [S]    (number of chunks of sequences 0..r) - 1: r's last
+ *                              chunk when r has new tokens; equal to r-1's entry
+ *                              (or -1) when it has none.
+ *   chunk_block_col     [K]    absolute position of chunk k's last token / chunk_size
+ *                              (may be NULL).
+ *   init_slot           [S]    slot r's initial state is read from, or null_block_id
+ *                              (may be NULL).  "all" mode: block_table[r,
+ *                              (num_computed-1)/chunk_size]; default mode:
+ *                              state_indices[r].  Only when has_initial_states[r].
+ *   chunk_slot          [K]    slot chunk k's end state is written to, or
+ *                              null_block_id (may be NULL).  "all" mode:
+ *                              block_table[seq, chunk_block_col]; default mode:
+ *                              state_indices[seq] for the sequence's last chunk.
+ *   num_chunks_out             K.
+ * Errors: SSD_ERR_INVALID_ARG for bad sizes, a decreasing cu_seqlens, negative
+ * num_computed_tokens, has_initial_states with num_computed_tokens == 0 in
+ * "all" mode, or a block column >= block_table_cols; SSD_ERR_WORKSPACE when
+ * max_chunks is too small.  Outputs are unspecified after an error.
+ */
+SSD_API ssd_status_t ssd_chunk_metadata(int32_t num_seqs, int32_t chunk_size, const int32_t *cu_seqlens,
+                                const int32_t *num_computed_tokens,
+                                const uint8_t *has_initial_states, const int32_t *block_table,
+                                int64_t block_table_stride, int32_t block_table_cols,
+                                const int32_t *state_indices, int32_t null_block_id,
+                                int32_t max_chunks, int32_t *cu_chunk_seqlens, int32_t *seq_idx,
+                                int32_t *last_chunk_indices, int32_t *chunk_block_col,
+                                int32_t *init_slot, int32_t *chunk_slot, int32_t *num_chunks_out);
+
+/* ------------------------------------------------------------------------ *
+ * Varlen SSD prefill (device)
+ *
+ * The chunked scan of "[vllm] vLLM Mamba2 SSD 커널 웜업", section
+ * "mamba_mixer2.py 변경 사항 (핵심)" (mamba_chunk_scan_combined_varlen with
+ * cu_seqlens, cu_chunk_seqlens, last_chunk_indices, seq_idx, optional initial
+ * states, dt_softplus, dt_limit, fp32 state), run for every packed sequence,
+ * storing the state at the end of every chunk (prefix caching, "청크 기반
+ * 프리픽스 캐싱" of the Mamba (SSM) page).
+ * ------------------------------------------------------------------------ */
+typedef struct ssd_prefill_args {
+    int32_t total_tokens; /* T = cu_seqlens[S] */
+    int32_t num_seqs;     /* S */
+    int32_t num_chunks;   /* K = cu_chunk_seqlens entries - 1 */
+    int32_t nheads;       /* H */
+    int32_t headdim;      /* P */
+    int32_t dstate;       /* N */
+    int32_t ngroups;      /* G, divides H */
+    int32_t chunk_size;   /* Q (informational; the chunks come from cu_chunk_seqlens) */
+    int32_t dtype;        /* ssd_dtype_t of x, dt, B, C and y */
+    int32_t dt_softplus;  /* nonzero: delta = softplus(dt + dt_bias) before the clamp */
+    float dt_min, dt_max; /* dt_limit clamp; (0, +inf) leaves softplus output as is */
+    int32_t num_slots;    /* rows of state_cache */
+    int32_t null_block_id;
+    /* device pointers */
+    const void *x;       /* [T, H, P]  dtype, 16-byte aligned */
+    const void *dt;      /* [T, H]     dtype */
+    const void *B;       /* [T, G, N]  dtype, 16-byte aligned */
+    const void *C;       /* [T, G, N]  dtype, 16-byte aligned */
+    const void *z;       /* gate; must be NULL (SSD_ERR_UNSUPPORTED otherwise) */
+    const float *A;      /* [H] (negative for a decaying state) */
+    const float *D;      /* [H] or NULL (no skip term) */
+    const float *dt_bias; /* [H] or NULL (zero) */
+    const int32_t *cu_seqlens;         /* [S+1] */
+    const int32_t *cu_chunk_seqlens;   /* [K+1] */
+    const int32_t *seq_idx;            /* [K] */
+    const int32_t *last_chunk_indices; /* [S] */
+    const int32_t *init_slot;  /* [S] or NULL (no initial states) */
+    const int32_t *chunk_slot; /* [K] or NULL (no state output) */
+    float *state_cache;        /* [num_slots, H, P, N] fp32, 16-byte aligned; may be NULL
+                                  when init_slot and chunk_slot are both NULL */
+    void *y;                   /* [T, H, P] dtype, 16-byte aligned, written for every token */
+    uint32_t *err_word;        /* device word or NULL */
+} ssd_prefill_args;
+
+/* Bytes of device workspace ssd_prefill_varlen needs for these arguments
+ * (sizes only are read).  0 on invalid sizes. */
+SSD_API size_t ssd_prefill_workspace_size(const ssd_prefill_args *args);
+
+/* Number of CUDA kernels one ssd_prefill_varlen call with these arguments
+ * launches (0 for an empty call, -1 on invalid sizes).  Host only. */
+SSD_API int32_t ssd_prefill_kernel_count(const ssd_prefill_args *args);
+
+/*
+ * Runs the prefill.  workspace: device memory of at least
+ * ssd_prefill_workspace_size(args) bytes, 256-byte aligned, caller-owned,
+ * no initial contents required, not shared with a concurrent call.
+ * Preconditions checked on the host: sizes > 0 (T, K may be 0: nothing
+ * happens), H % G == 0, headdim <= 256, dstate <= 256, the pointers required
+ * by the sizes are non-NULL, the alignments above.  Returns SSD_ERR_CUDA if a
+ * launch fails.
+ */
+SSD_API ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *args, void *workspace,
+                                size_t workspace_bytes, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Decode state update (device)
+ *
+ * "decode는 순차적 갱신" (decode is a sequential update, "왜 이 설계인가"
+ * item 2 of the Mamba (SSM) page), with the state-index table of
+ * "MetadataBuilder 초기화" ([batch, 1 + num_spec] or [batch, max_blocks]),
+ * the CUDA-graph padding of "CUDA Graph 지원" (padded rows hold
+ * NULL_BLOCK_ID and are skipped) and the speculative-decode checkpoint of
+ * "왜 이 설계인가" item 4 (num_accepted_tokens picks the state to resume from).
+ * ------------------------------------------------------------------------ */
+typedef struct ssm_decode_args {
+    int32_t batch;          /* R, rows of state_indices (live + padding) */
+    int32_t tokens_per_req; /* 1 + num_speculative_tokens */
+    int32_t nheads, headdim, dstate, ngroups;
+    int32_t dtype;          /* ssd_dtype_t of x, dt, B, C and y */
+    int32_t dt_softplus;
+    float dt_min, dt_max;
+    int32_t num_slots;
+    int32_t null_block_id;
+    int32_t state_indices_cols; /* columns of a state_indices row, >= tokens_per_req */
+    const void *x;  /* [R * tokens_per_req, H, P]; token k of request r is row r*tpr + k */
+    const void *dt; /* [R * tokens_per_req, H] */
+    const void *B;  /* [R * tokens_per_req, G, N] */
+    const void *C;  /* [R * tokens_per_req, G, N] */
+    const void *z;  /* must be NULL */
+    const float *A, *D, *dt_bias;      /* [H]; D and dt_bias may be NULL */
+    float *state_cache;                /* [num_slots, H, P, N] fp32, updated in place */
+    const int32_t *state_indices;      /* [R, state_indices_cols] */
+    const int32_t *num_accepted_tokens; /* [R] or NULL (all 0): request r resumes from the
+                                          state in column num_accepted_tokens[r] */
+    void *y;                 /* [R * tokens_per_req, H, P]; rows of skipped requests untouched */
+    uint32_t *err_word;      /* device word or NULL */
+} ssm_decode_args;
+
+/*
+ * Request r with read slot rs = state_indices[r, num_accepted_tokens[r]]:
+ * if rs == null_block_id the request is padding and nothing of it is read or
+ * written.  Otherwise its state is read from rs, the tokens_per_req tokens are
+ * applied in order, y is written for each, and the state after token k is
+ * stored to state_indices[r, k] unless that id is null.  The read happens
+ * before any write (the read slot may be one of the write slots).
+ * Host checks as for prefill, plus tokens_per_req >= 1,
+ * state_indices_cols >= tokens_per_req.
+ */
+SSD_API ssd_status_t ssm_decode_update(const ssm_decode_args *args, ssd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_GB300_SSD_H */

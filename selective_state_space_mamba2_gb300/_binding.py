@@ -1,0 +1,301 @@
+"""ctypes binding of ``include/ssd.h``: argument marshalling only.
+
+Every numeric step runs in ``libssd_gb300.so``; torch supplies device memory
+and the current stream.  The library is loaded on first use and a missing
+build raises immediately -- there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssd_gb300.so")
+
+SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE, SSD_ERR_CUDA = range(5)
+SSD_F32, SSD_BF16 = 0, 1
+DEVERR_SLOT, DEVERR_METADATA, DEVERR_COLUMN, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+EXPORTED_SYMBOLS = ("ssd_status_string", "ssd_abi_version", "ssd_max_chunks", "ssd_chunk_metadata",
+                    "ssd_prefill_workspace_size", "ssd_prefill_kernel_count", "ssd_prefill_varlen",
+                    "ssm_decode_update")
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_f32 = ctypes.c_float
+
+
+class PrefillArgs(ctypes.Structure):
+    _fields_ = [("total_tokens", _i32), ("num_seqs", _i32), ("num_chunks", _i32), ("nheads", _i32),
+                ("headdim", _i32), ("dstate", _i32), ("ngroups", _i32), ("chunk_size", _i32),
+                ("dtype", _i32), ("dt_softplus", _i32), ("dt_min", _f32), ("dt_max", _f32),
+                ("num_slots", _i32), ("null_block_id", _i32),
+                ("x", _vp), ("dt", _vp), ("B", _vp), ("C", _vp), ("z", _vp), ("A", _vp), ("D", _vp),
+                ("dt_bias", _vp), ("cu_seqlens", _vp), ("cu_chunk_seqlens", _vp), ("seq_idx", _vp),
+                ("last_chunk_indices", _vp), ("init_slot", _vp), ("chunk_slot", _vp),
+                ("state_cache", _vp), ("y", _vp), ("err_word", _vp)]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [("batch", _i32), ("tokens_per_req", _i32), ("nheads", _i32), ("headdim", _i32),
+                ("dstate", _i32), ("ngroups", _i32), ("dtype", _i32), ("dt_softplus", _i32),
+                ("dt_min", _f32), ("dt_max", _f32), ("num_slots", _i32), ("null_block_id", _i32),
+                ("state_indices_cols", _i32),
+                ("x", _vp), ("dt", _vp), ("B", _vp), ("C", _vp), ("z", _vp), ("A", _vp), ("D", _vp),
+                ("dt_bias", _vp), ("state_cache", _vp), ("state_indices", _vp),
+                ("num_accepted_tokens", _vp), ("y", _vp), ("err_word", _vp)]
+
+
+class SSDError(RuntimeError):
+    def __init__(self, fn, code):
+        name = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED",
+                3: "SSD_ERR_WORKSPACE", 4: "SSD_ERR_CUDA"}.get(code, str(code))
+        super().__init__("%s returned %s" % (fn, name))
+        self.code = code
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("%s is missing: build it with __graft_entry__.build() (nvcc, sm_103a)"
+                               % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        ip = ctypes.POINTER(ctypes.c_int32)
+        L.ssd_status_string.restype = ctypes.c_char_p
+        L.ssd_status_string.argtypes = [ctypes.c_int]
+        L.ssd_abi_version.restype = _i32
+        L.ssd_max_chunks.restype = _i32
+        L.ssd_max_chunks.argtypes = [_i32, _i32, _i32]
+        L.ssd_chunk_metadata.restype = ctypes.c_int
+        L.ssd_chunk_metadata.argtypes = [_i32, _i32, ip, ip, ctypes.POINTER(ctypes.c_uint8), ip,
+                                         ctypes.c_int64, _i32, ip, _i32, _i32, ip, ip, ip, ip, ip,
+                                         ip, ip]
+        L.ssd_prefill_workspace_size.restype = ctypes.c_size_t
+        L.ssd_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
+        L.ssd_prefill_kernel_count.restype = _i32
+        L.ssd_prefill_kernel_count.argtypes = [ctypes.POINTER(PrefillArgs)]
+        L.ssd_prefill_varlen.restype = ctypes.c_int
+        L.ssd_prefill_varlen.argtypes = [ctypes.POINTER(PrefillArgs), _vp, ctypes.c_size_t, _vp]
+        L.ssm_decode_update.restype = ctypes.c_int
+        L.ssm_decode_update.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        _lib = L
+    return _lib
+
+
+# ----------------------------------------------------------------- helpers --
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return SSD_BF16
+    if t.dtype == torch.float32:
+        return SSD_F32
+    raise ValueError("x/dt/B/C must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _dev(t, name, dtype=None, required=True):
+    if t is None:
+        if required:
+            raise ValueError("%s is required" % name)
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t.data_ptr()
+
+
+def _host_i32(a, name):
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda:
+            raise ValueError("%s must be host memory" % name)
+        a = a.numpy()
+    return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+
+
+def _ptr(a, ctype=ctypes.c_int32):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+# ----------------------------------------------------------------- API ------
+
+def ssd_max_chunks(num_seqs, total_tokens, chunk_size):
+    return int(lib().ssd_max_chunks(int(num_seqs), int(total_tokens), int(chunk_size)))
+
+
+def ssd_chunk_metadata(cu_seqlens, chunk_size, num_computed_tokens=None, has_initial_states=None,
+                       block_table=None, state_indices=None, null_block_id=0):
+    """Host chunk metadata and slot routing (see ``ssd_chunk_metadata`` in ssd.h).
+
+    All inputs are host arrays; returns a dict of int32 numpy arrays:
+    cu_chunk_seqlens [K+1], seq_idx [K], last_chunk_indices [S],
+    chunk_block_col [K], init_slot [S], chunk_slot [K].
+    """
+    cu = _host_i32(cu_seqlens, "cu_seqlens")
+    S = cu.shape[0] - 1
+    T = int(cu[-1])
+    nc = _host_i32(num_computed_tokens, "num_computed_tokens")
+    has = None
+    if has_initial_states is not None:
+        h = has_initial_states.numpy() if isinstance(has_initial_states, torch.Tensor) else has_initial_states
+        has = np.ascontiguousarray(np.asarray(h).astype(bool), dtype=np.uint8)
+    bt = _host_i32(block_table, "block_table")
+    si = _host_i32(state_indices, "state_indices")
+    maxk = max(ssd_max_chunks(S, T, chunk_size), 0)
+    out = dict(cu_chunk_seqlens=np.zeros(maxk + 1, np.int32), seq_idx=np.zeros(max(maxk, 1), np.int32),
+               last_chunk_indices=np.zeros(max(S, 1), np.int32),
+               chunk_block_col=np.zeros(max(maxk, 1), np.int32), init_slot=np.zeros(max(S, 1), np.int32),
+               chunk_slot=np.zeros(max(maxk, 1), np.int32))
+    k = ctypes.c_int32(0)
+    rc = lib().ssd_chunk_metadata(
+        S, int(chunk_size), _ptr(cu), _ptr(nc), _ptr(has, ctypes.c_uint8), _ptr(bt),
+        0 if bt is None else bt.shape[1], 0 if bt is None else bt.shape[1], _ptr(si), int(null_block_id),
+        maxk, _ptr(out["cu_chunk_seqlens"]), _ptr(out["seq_idx"]), _ptr(out["last_chunk_indices"]),
+        _ptr(out["chunk_block_col"]), _ptr(out["init_slot"]), _ptr(out["chunk_slot"]), ctypes.byref(k))
+    if rc != SSD_OK:
+        raise SSDError("ssd_chunk_metadata", rc)
+    K = k.value
+    return dict(cu_chunk_seqlens=out["cu_chunk_seqlens"][:K + 1].copy(), seq_idx=out["seq_idx"][:K].copy(),
+                last_chunk_indices=out["last_chunk_indices"][:S].copy(),
+                chunk_block_col=out["chunk_block_col"][:K].copy(), init_slot=out["init_slot"][:S].copy(),
+                chunk_slot=out["chunk_slot"][:K].copy())
+
+
+def prefill_args(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices, out,
+                 init_slot=None, chunk_slot=None, state_cache=None, D=None, dt_bias=None, z=None,
+                 dt_softplus=True, dt_limit=(0.0, math.inf), null_block_id=0, chunk_size=None,
+                 err_word=None):
+    """Fills a ``PrefillArgs`` from device tensors (validating shapes and dtypes)."""
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    dtype = _dtype_code(x)
+    for name, t, shp in (("dt", dt, (T, H)), ("B", B, (T, G, N)), ("C", C, (T, G, N)), ("out", out, (T, H, P))):
+        if tuple(t.shape) != shp or t.dtype != x.dtype:
+            raise ValueError("%s must be %s of shape %s" % (name, x.dtype, shp))
+    S = cu_seqlens.shape[0] - 1
+    K = cu_chunk_seqlens.shape[0] - 1
+    a = PrefillArgs()
+    a.total_tokens, a.num_seqs, a.num_chunks = T, S, K
+    a.nheads, a.headdim, a.dstate, a.ngroups = H, P, N, G
+    a.chunk_size = int(chunk_size) if chunk_size else 0
+    a.dtype = dtype
+    a.dt_softplus = int(bool(dt_softplus))
+    a.dt_min, a.dt_max = float(dt_limit[0]), float(dt_limit[1])
+    a.null_block_id = int(null_block_id)
+    a.x, a.dt, a.B, a.C, a.y = (_dev(x, "x"), _dev(dt, "dt"), _dev(B, "B"), _dev(C, "C"), _dev(out, "out"))
+    a.z = _dev(z, "z", required=False)
+    a.A = _dev(A, "A", torch.float32)
+    a.D = _dev(D, "D", torch.float32, required=False)
+    a.dt_bias = _dev(dt_bias, "dt_bias", torch.float32, required=False)
+    a.cu_seqlens = _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    a.cu_chunk_seqlens = _dev(cu_chunk_seqlens, "cu_chunk_seqlens", torch.int32)
+    a.seq_idx = _dev(seq_idx, "seq_idx", torch.int32, required=False)
+    a.last_chunk_indices = _dev(last_chunk_indices, "last_chunk_indices", torch.int32)
+    a.init_slot = _dev(init_slot, "init_slot", torch.int32, required=False)
+    a.chunk_slot = _dev(chunk_slot, "chunk_slot", torch.int32, required=False)
+    if state_cache is not None:
+        if state_cache.dtype != torch.float32 or tuple(state_cache.shape[1:]) != (H, P, N):
+            raise ValueError("state_cache must be float32 [slots, %d, %d, %d]" % (H, P, N))
+        a.state_cache = _dev(state_cache, "state_cache")
+        a.num_slots = state_cache.shape[0]
+    a.err_word = _dev(err_word, "err_word", required=False)
+    if a.chunk_size == 0:
+        a.chunk_size = 1
+    return a
+
+
+def ssd_prefill_workspace_size(args):
+    return int(lib().ssd_prefill_workspace_size(ctypes.byref(args)))
+
+
+def ssd_prefill_kernel_count(args):
+    return int(lib().ssd_prefill_kernel_count(ctypes.byref(args)))
+
+
+def ssd_prefill_varlen(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices,
+                       out=None, init_slot=None, chunk_slot=None, state_cache=None, D=None,
+                       dt_bias=None, z=None, dt_softplus=True, dt_limit=(0.0, math.inf),
+                       null_block_id=0, chunk_size=None, workspace=None, err_word=None, stream=None):
+    """Varlen SSD prefill on device tensors; returns ``out`` ([T,H,P], x's dtype).
+
+    ``workspace`` (uint8 CUDA tensor) is allocated with torch when omitted.
+    """
+    if out is None:
+        out = torch.empty_like(x)
+    a = prefill_args(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices, out,
+                     init_slot, chunk_slot, state_cache, D, dt_bias, z, dt_softplus, dt_limit,
+                     null_block_id, chunk_size, err_word)
+    need = ssd_prefill_workspace_size(a)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    rc = lib().ssd_prefill_varlen(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
+                                  workspace.numel(), _stream(stream))
+    if rc != SSD_OK:
+        raise SSDError("ssd_prefill_varlen", rc)
+    return out
+
+
+def decode_args(x, dt, A, B, C, state_cache, state_indices, out, num_accepted_tokens=None, D=None,
+                dt_bias=None, z=None, dt_softplus=True, dt_limit=(0.0, math.inf), null_block_id=0,
+                err_word=None):
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    R, cols = state_indices.shape
+    if R == 0 or T % R:
+        raise ValueError("x rows must be a multiple of state_indices rows")
+    for name, t, shp in (("dt", dt, (T, H)), ("B", B, (T, G, N)), ("C", C, (T, G, N)), ("out", out, (T, H, P))):
+        if tuple(t.shape) != shp or t.dtype != x.dtype:
+            raise ValueError("%s must be %s of shape %s" % (name, x.dtype, shp))
+    if state_cache.dtype != torch.float32 or tuple(state_cache.shape[1:]) != (H, P, N):
+        raise ValueError("state_cache must be float32 [slots, %d, %d, %d]" % (H, P, N))
+    a = DecodeArgs()
+    a.batch, a.tokens_per_req = R, T // R
+    a.nheads, a.headdim, a.dstate, a.ngroups = H, P, N, G
+    a.dtype = _dtype_code(x)
+    a.dt_softplus = int(bool(dt_softplus))
+    a.dt_min, a.dt_max = float(dt_limit[0]), float(dt_limit[1])
+    a.num_slots = state_cache.shape[0]
+    a.null_block_id = int(null_block_id)
+    a.state_indices_cols = cols
+    a.x, a.dt, a.B, a.C, a.y = (_dev(x, "x"), _dev(dt, "dt"), _dev(B, "B"), _dev(C, "C"), _dev(out, "out"))
+    a.z = _dev(z, "z", required=False)
+    a.A = _dev(A, "A", torch.float32)
+    a.D = _dev(D, "D", torch.float32, required=False)
+    a.dt_bias = _dev(dt_bias, "dt_bias", torch.float32, required=False)
+    a.state_cache = _dev(state_cache, "state_cache")
+    a.state_indices = _dev(state_indices, "state_indices", torch.int32)
+    a.num_accepted_tokens = _dev(num_accepted_tokens, "num_accepted_tokens", torch.int32, required=False)
+    a.err_word = _dev(err_word, "err_word", required=False)
+    return a
+
+
+def ssm_decode_update(x, dt, A, B, C, state_cache, state_indices, num_accepted_tokens=None, out=None,
+                      D=None, dt_bias=None, z=None, dt_softplus=True, dt_limit=(0.0, math.inf),
+                      null_block_id=0, err_word=None, stream=None):
+    """In-place decode update of ``state_cache``; returns ``out`` ([R*tpr,H,P])."""
+    if out is None:
+        out = torch.empty_like(x)
+    a = decode_args(x, dt, A, B, C, state_cache, state_indices, out, num_accepted_tokens, D, dt_bias, z,
+                    dt_softplus, dt_limit, null_block_id, err_word)
+    rc = lib().ssm_decode_update(ctypes.byref(a), _stream(stream))
+    if rc != SSD_OK:
+        raise SSDError("ssm_decode_update", rc)
+    return out

@@ -1,0 +1,95 @@
+// C-ABI entry points: host-side argument checks, workspace carving, dispatch.
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ssd_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+bool dtype_ok(int32_t d) { return d == SSD_F32 || d == SSD_BF16; }
+
+bool limits_ok(float lo, float hi) { return !std::isnan(lo) && !std::isnan(hi) && lo <= hi; }
+
+// sizes shared by prefill and decode
+bool dims_ok(int32_t H, int32_t P, int32_t N, int32_t G) {
+    return H > 0 && P > 0 && N > 0 && G > 0 && H % G == 0 && P <= 256 && N <= 256;
+}
+
+ssd_status_t check_prefill(const ssd_prefill_args *a) {
+    if (!a) return SSD_ERR_INVALID_ARG;
+    if (a->total_tokens < 0 || a->num_seqs < 0 || a->num_chunks < 0) return SSD_ERR_INVALID_ARG;
+    if (!dims_ok(a->nheads, a->headdim, a->dstate, a->ngroups)) return SSD_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype) || !limits_ok(a->dt_min, a->dt_max)) return SSD_ERR_INVALID_ARG;
+    if (a->z) return SSD_ERR_UNSUPPORTED;
+    if (a->num_chunks > 0 && (a->total_tokens == 0 || a->num_seqs == 0)) return SSD_ERR_INVALID_ARG;
+    if (a->total_tokens > 0 && a->num_chunks == 0) return SSD_ERR_INVALID_ARG;
+    if (a->total_tokens == 0) return SSD_OK;
+    if (!a->x || !a->dt || !a->B || !a->C || !a->A || !a->y || !a->cu_seqlens ||
+        !a->cu_chunk_seqlens || !a->last_chunk_indices)
+        return SSD_ERR_INVALID_ARG;
+    if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->y))
+        return SSD_ERR_INVALID_ARG;
+    if ((a->init_slot || a->chunk_slot) && (!a->state_cache || a->num_slots <= 0 || !aligned16(a->state_cache)))
+        return SSD_ERR_INVALID_ARG;
+    return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" const char *ssd_status_string(ssd_status_t s) {
+    switch (s) {
+        case SSD_OK: return "SSD_OK";
+        case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG";
+        case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED";
+        case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE";
+        case SSD_ERR_CUDA: return "SSD_ERR_CUDA";
+    }
+    return "SSD_ERR_UNKNOWN";
+}
+
+extern "C" int32_t ssd_abi_version(void) { return SSD_ABI_VERSION; }
+
+extern "C" size_t ssd_prefill_workspace_size(const ssd_prefill_args *a) {
+    if (check_prefill(a) != SSD_OK) return 0;
+    if (a->total_tokens == 0) return 0;
+    return ssd::simt_prefill_workspace(*a, nullptr, nullptr);
+}
+
+extern "C" int32_t ssd_prefill_kernel_count(const ssd_prefill_args *a) {
+    if (check_prefill(a) != SSD_OK) return -1;
+    if (a->total_tokens == 0) return 0;
+    return 4;
+}
+
+extern "C" ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *a, void *workspace,
+                                           size_t workspace_bytes, ssd_stream_t stream) {
+    const ssd_status_t st = check_prefill(a);
+    if (st != SSD_OK || a->total_tokens == 0) return st;
+    if (!ssd::simt_prefill_supported(*a)) return SSD_ERR_UNSUPPORTED;
+    const size_t need = ssd::simt_prefill_workspace(*a, nullptr, nullptr);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SSD_ERR_WORKSPACE;
+    ssd::PrefillWorkspace ws;
+    ssd::simt_prefill_workspace(*a, &ws, workspace);
+    return from_cuda(ssd::simt_prefill_launch(*a, ws, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" ssd_status_t ssm_decode_update(const ssm_decode_args *a, ssd_stream_t stream) {
+    if (!a) return SSD_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->tokens_per_req < 1 || a->state_indices_cols < a->tokens_per_req)
+        return SSD_ERR_INVALID_ARG;
+    if (!dims_ok(a->nheads, a->headdim, a->dstate, a->ngroups)) return SSD_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype) || !limits_ok(a->dt_min, a->dt_max)) return SSD_ERR_INVALID_ARG;
+    if (a->z) return SSD_ERR_UNSUPPORTED;
+    if (a->batch == 0) return SSD_OK;
+    if (!a->x || !a->dt || !a->B || !a->C || !a->A || !a->y || !a->state_cache || !a->state_indices ||
+        a->num_slots <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (!aligned16(a->state_cache) || a->dstate % 4 != 0) return SSD_ERR_INVALID_ARG;
+    if (!ssd::decode_supported(*a)) return SSD_ERR_UNSUPPORTED;
+    return from_cuda(ssd::decode_launch(*a, reinterpret_cast<cudaStream_t>(stream)));
+}

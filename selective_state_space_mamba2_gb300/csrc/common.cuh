@@ -1,0 +1,67 @@
+// Shared device helpers of the SSD library (internal header).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// ---- element access -------------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+template <typename T> __device__ __forceinline__ float ldg_f32(const T *p) { return to_f32(__ldg(p)); }
+
+// ---- the per-token step size ----------------------------------------------
+// delta = clamp(softplus(dt + dt_bias), dt_min, dt_max).  softplus(v) is taken
+// as v itself above 20, where log1p(exp(v)) - v < 2.1e-9 * v (below fp32
+// resolution); CUDA's expf / log1pf are called, not re-derived.
+__device__ __forceinline__ float step_delta(float dt_plus_bias, int dt_softplus, float dt_min,
+                                            float dt_max) {
+    float d = dt_plus_bias;
+    if (dt_softplus) d = d > 20.f ? d : log1pf(__expf(d));
+    return fminf(fmaxf(d, dt_min), dt_max);
+}
+
+// ---- device error word ------------------------------------------------------
+__device__ __forceinline__ void report(uint32_t *err, uint32_t bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// true when `slot` may be accessed; reports out-of-range ids (null is not an error)
+__device__ __forceinline__ bool slot_usable(int32_t slot, int32_t null_id, int32_t num_slots,
+                                            uint32_t *err) {
+    if (slot == null_id) return false;
+    if (slot < 0 || slot >= num_slots) {
+        report(err, SSD_DEVERR_SLOT);
+        return false;
+    }
+    return true;
+}
+
+}  // namespace ssd
+
+// ---- internal launchers (C++ linkage, not part of the ABI) -------------------
+namespace ssd {
+struct PrefillWorkspace {
+    float *delta;        // [H, T]
+    float *cumlog;       // [H, T] inclusive in-chunk cumsum of delta * A
+    float *chunk_state;  // [K, H, P, N]
+    float *state_in;     // [K, H, P, N]
+};
+size_t simt_prefill_workspace(const ssd_prefill_args &a, PrefillWorkspace *ws, void *base);
+cudaError_t simt_prefill_launch(const ssd_prefill_args &a, const PrefillWorkspace &ws,
+                                cudaStream_t s);
+bool simt_prefill_supported(const ssd_prefill_args &a);
+
+bool decode_supported(const ssm_decode_args &a);
+cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s);
+}  // namespace ssd

@@ -1,0 +1,147 @@
+// Decode state update: one CTA per (request, head), state held in registers.
+//
+// "[vLLM] Mamba (SSM): 선형 시간 복잡도 시퀀스 모델링": decode is a sequential
+// update ("왜 이 설계인가" item 2) through the state-index table of
+// "MetadataBuilder 초기화"; padded CUDA-graph rows hold NULL_BLOCK_ID
+// ("CUDA Graph 지원") and are skipped; with speculative tokens,
+// num_accepted_tokens selects the checkpoint to resume from ("왜 이 설계인가"
+// item 4) and every token's state is stored to its own column.
+//
+// Memory behaviour: per live (request, head) the fp32 state [P, N] is read
+// once (float4, a warp covers 512 contiguous bytes) and written once per
+// token whose column slot is not null.  That traffic is the whole algorithmic
+// cost, so the kernel is HBM-bound; the arithmetic (one exp per token, one
+// FMA pair per state element, a warp-shuffle reduction over dstate for y)
+// hides under it.
+#include "common.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename Tin, int VPT>
+__global__ void __launch_bounds__(kThreads)
+    ssm_decode_kernel(const ssm_decode_args a) {
+    const int r = blockIdx.x;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int H = a.nheads, P = a.headdim, N = a.dstate;
+    const int g = h / (H / a.ngroups);
+    const int tpr = a.tokens_per_req;
+
+    const int col = a.num_accepted_tokens ? a.num_accepted_tokens[r] : 0;
+    if (col < 0 || col >= a.state_indices_cols) {
+        if (tid == 0 && h == 0) report(a.err_word, SSD_DEVERR_COLUMN);
+        return;
+    }
+    const int32_t *row_slots = a.state_indices + (size_t)r * a.state_indices_cols;
+    const int32_t rs = row_slots[col];
+    if (rs == a.null_block_id) return;  // CUDA-graph padding row
+    if (rs < 0 || rs >= a.num_slots) {
+        if (tid == 0 && h == 0) report(a.err_word, SSD_DEVERR_SLOT);
+        return;
+    }
+
+    __shared__ float sx[256], sB[256], sC[256], sy[256];
+
+    const int PN = P * N;
+    const int nvec = PN >> 2;  // float4 chunks; N % 4 == 0
+    const size_t head_off = (size_t)h * PN;
+    float4 s[VPT];
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(a.state_cache + (size_t)rs * H * PN + head_off);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int e = tid + i * kThreads;
+            s[i] = e < nvec ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    // rows of dstate/4 chunks: a segment of `seg` lanes shares one p
+    const int quads = N >> 2;
+    const int seg = quads < 32 ? quads : 32;
+
+    const float A = a.A[h];
+    const float Dh = a.D ? a.D[h] : 0.f;
+    const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
+    const Tin *x = static_cast<const Tin *>(a.x);
+    const Tin *dtp = static_cast<const Tin *>(a.dt);
+    const Tin *Bp = static_cast<const Tin *>(a.B);
+    const Tin *Cp = static_cast<const Tin *>(a.C);
+    Tin *y = static_cast<Tin *>(a.y);
+
+    for (int k = 0; k < tpr; ++k) {
+        const size_t row = (size_t)r * tpr + k;
+        __syncthreads();  // the previous token's readers of sx/sy are done
+        for (int j = tid; j < P; j += kThreads) {
+            sx[j] = ldg_f32(x + (row * H + h) * P + j);
+            sy[j] = 0.f;
+        }
+        for (int j = tid; j < N; j += kThreads) {
+            sB[j] = ldg_f32(Bp + (row * a.ngroups + g) * N + j);
+            sC[j] = ldg_f32(Cp + (row * a.ngroups + g) * N + j);
+        }
+        __syncthreads();
+        const float delta = step_delta(ldg_f32(dtp + row * H + h) + bias, a.dt_softplus, a.dt_min, a.dt_max);
+        const float decay = __expf(delta * A);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int e = tid + i * kThreads;
+            float part = 0.f;
+            int p = 0;
+            if (e < nvec) {
+                p = e / quads;
+                const int n = (e - p * quads) << 2;
+                const float dx = delta * sx[p];
+                s[i].x = fmaf(decay, s[i].x, dx * sB[n + 0]);
+                s[i].y = fmaf(decay, s[i].y, dx * sB[n + 1]);
+                s[i].z = fmaf(decay, s[i].z, dx * sB[n + 2]);
+                s[i].w = fmaf(decay, s[i].w, dx * sB[n + 3]);
+                part = s[i].x * sC[n] + s[i].y * sC[n + 1] + s[i].z * sC[n + 2] + s[i].w * sC[n + 3];
+            }
+            // segmented reduction over the lanes that share p
+            for (int off = seg >> 1; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+            if (e < nvec && (threadIdx.x & (seg - 1)) == 0) atomicAdd(&sy[p], part);
+        }
+        __syncthreads();
+        for (int j = tid; j < P; j += kThreads)
+            y[(row * H + h) * P + j] = from_f32<Tin>(sy[j] + Dh * sx[j]);
+        const int32_t ws = row_slots[k];
+        if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr)) {
+            float4 *dst = reinterpret_cast<float4 *>(a.state_cache + (size_t)ws * H * PN + head_off);
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int e = tid + i * kThreads;
+                if (e < nvec) dst[e] = s[i];
+            }
+        }
+    }
+}
+
+template <typename Tin>
+cudaError_t launch_typed(const ssm_decode_args &a, cudaStream_t st) {
+    const int nvec = a.headdim * a.dstate / 4;
+    const int vpt = (nvec + kThreads - 1) / kThreads;
+    dim3 grid(a.batch, a.nheads);
+    if (vpt <= 1) ssm_decode_kernel<Tin, 1><<<grid, kThreads, 0, st>>>(a);
+    else if (vpt <= 2) ssm_decode_kernel<Tin, 2><<<grid, kThreads, 0, st>>>(a);
+    else if (vpt <= 4) ssm_decode_kernel<Tin, 4><<<grid, kThreads, 0, st>>>(a);
+    else if (vpt <= 8) ssm_decode_kernel<Tin, 8><<<grid, kThreads, 0, st>>>(a);
+    else ssm_decode_kernel<Tin, 16><<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_supported(const ssm_decode_args &a) {
+    const int N = a.dstate;
+    const bool n_ok = (N % 128 == 0) || (N >= 4 && (N & (N - 1)) == 0);
+    return n_ok && a.headdim <= 256 && N <= 256 && a.headdim * N <= 16 * 4 * kThreads;
+}
+
+cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s) {
+    if (a.dtype == SSD_BF16) return launch_typed<__nv_bfloat16>(a, s);
+    return launch_typed<float>(a, s);
+}
+
+}  // namespace ssd

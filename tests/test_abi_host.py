@@ -1,0 +1,158 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every symbol the header declares, the host chunk metadata matches the
+oracle's per-token definition bit for bit, and invalid arguments are refused
+before anything is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import selective_state_space_mamba2_gb300 as ssd
+from selective_state_space_mamba2_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ssd.build()
+    return ssd.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"SSD_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert set(B.EXPORTED_SYMBOLS) <= set(declared)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert lib.ssd_abi_version() == 1
+    assert lib.ssd_status_string(3) == b"SSD_ERR_WORKSPACE"
+
+
+def test_max_chunks_bound(lib):
+    assert ssd.ssd_max_chunks(1, 0, 4) == 0
+    assert ssd.ssd_max_chunks(2, 4, 4) == 4
+    assert ssd.ssd_max_chunks(3, 100, 16) == 6 + 7
+    assert ssd.ssd_max_chunks(-1, 5, 4) == -1
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_metadata_matches_oracle_bit_exact(lib, oracle_lib, seed):
+    rng = np.random.default_rng(seed)
+    S = int(rng.integers(1, 40))
+    Q = int(rng.choice([1, 5, 16, 64, 256, 2048]))
+    lens = rng.integers(0, 4 * Q + 9, S)
+    nc = rng.integers(0, 8 * Q + 3, S)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    has = rng.integers(0, 2, S).astype(bool) & (nc > 0)
+    null = int(rng.choice([0, -1]))
+    cols = int(((nc + lens - 1) // Q).max()) + 2
+    bt = rng.permutation(np.arange(1, S * cols + 1)).reshape(S, cols).astype(np.int32)
+    m = ssd.ssd_chunk_metadata(cu, Q, nc, has, block_table=bt, null_block_id=null)
+    o = oracle_lib.chunk_metadata(cu, nc, Q)
+    for key in ("cu_chunk_seqlens", "seq_idx", "last_chunk_indices", "chunk_block_col"):
+        assert np.array_equal(m[key], o[key]), key
+    init, cslot = oracle_lib.prefill_slots(o, nc, Q, null, block_table=bt, has_initial_states=has)
+    assert np.array_equal(m["init_slot"], init) and np.array_equal(m["chunk_slot"], cslot)
+    si = rng.permutation(np.arange(1, S + 1)).astype(np.int32)
+    md = ssd.ssd_chunk_metadata(cu, Q, nc, has, state_indices=si, null_block_id=null)
+    init_d, cslot_d = oracle_lib.prefill_slots(o, nc, Q, null, state_indices=si, has_initial_states=has)
+    assert np.array_equal(md["init_slot"], init_d) and np.array_equal(md["chunk_slot"], cslot_d)
+
+
+def test_metadata_rejects_bad_input(lib):
+    with pytest.raises(B.SSDError) as e:
+        ssd.ssd_chunk_metadata([0, 5, 3], 4)
+    assert e.value.code == B.SSD_ERR_INVALID_ARG
+    with pytest.raises(B.SSDError):
+        ssd.ssd_chunk_metadata([1, 5], 4)
+    with pytest.raises(B.SSDError):
+        ssd.ssd_chunk_metadata([0, 5], 0)
+    with pytest.raises(B.SSDError):  # initial state but nothing computed ("all" mode)
+        ssd.ssd_chunk_metadata([0, 5], 4, [0], [True], block_table=np.ones((1, 4), np.int32))
+    with pytest.raises(B.SSDError):  # block column beyond the table
+        ssd.ssd_chunk_metadata([0, 9], 4, [0], block_table=np.ones((1, 2), np.int32))
+
+
+def _prefill_args(**over):
+    a = B.PrefillArgs()
+    a.total_tokens, a.num_seqs, a.num_chunks = 8, 1, 1
+    a.nheads, a.headdim, a.dstate, a.ngroups, a.chunk_size = 2, 4, 4, 1, 8
+    a.dtype, a.dt_softplus, a.dt_min, a.dt_max = B.SSD_F32, 1, 0.0, float("inf")
+    for f in ("x", "dt", "B", "C", "A", "y", "cu_seqlens", "cu_chunk_seqlens", "last_chunk_indices"):
+        setattr(a, f, 0x10000)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(ngroups=3), B.SSD_ERR_INVALID_ARG),
+    (dict(headdim=257), B.SSD_ERR_INVALID_ARG),
+    (dict(dtype=7), B.SSD_ERR_INVALID_ARG),
+    (dict(z=0x20000), B.SSD_ERR_UNSUPPORTED),
+    (dict(x=0x10008), B.SSD_ERR_INVALID_ARG),
+    (dict(x=None), B.SSD_ERR_INVALID_ARG),
+    (dict(dt_min=1.0, dt_max=0.5), B.SSD_ERR_INVALID_ARG),
+    (dict(num_chunks=0), B.SSD_ERR_INVALID_ARG),
+    (dict(init_slot=0x10000), B.SSD_ERR_INVALID_ARG),  # slots without a cache
+])
+def test_prefill_host_validation(lib, over, code):
+    a = _prefill_args(**over)
+    assert lib.ssd_prefill_varlen(ctypes.byref(a), None, 0, None) == code
+    assert lib.ssd_prefill_workspace_size(ctypes.byref(a)) == 0
+
+
+def test_prefill_workspace_too_small_is_refused(lib):
+    a = _prefill_args()
+    need = lib.ssd_prefill_workspace_size(ctypes.byref(a))
+    assert need > 0
+    assert lib.ssd_prefill_varlen(ctypes.byref(a), ctypes.c_void_p(0x100000), need - 1, None) == B.SSD_ERR_WORKSPACE
+    assert lib.ssd_prefill_varlen(ctypes.byref(a), ctypes.c_void_p(0x100010), need, None) == B.SSD_ERR_WORKSPACE
+
+
+def test_empty_prefill_is_a_no_op(lib):
+    a = _prefill_args(total_tokens=0, num_chunks=0)
+    assert lib.ssd_prefill_varlen(ctypes.byref(a), None, 0, None) == B.SSD_OK
+
+
+def _decode_args(**over):
+    a = B.DecodeArgs()
+    a.batch, a.tokens_per_req, a.nheads, a.headdim, a.dstate, a.ngroups = 2, 1, 2, 4, 8, 1
+    a.dtype, a.dt_softplus, a.dt_min, a.dt_max = B.SSD_BF16, 1, 0.0, float("inf")
+    a.num_slots, a.null_block_id, a.state_indices_cols = 4, 0, 1
+    for f in ("x", "dt", "B", "C", "A", "y", "state_cache", "state_indices"):
+        setattr(a, f, 0x10000)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(tokens_per_req=0), B.SSD_ERR_INVALID_ARG),
+    (dict(tokens_per_req=2), B.SSD_ERR_INVALID_ARG),  # fewer columns than tokens
+    (dict(ngroups=3), B.SSD_ERR_INVALID_ARG),
+    (dict(z=0x20000), B.SSD_ERR_UNSUPPORTED),
+    (dict(state_cache=0x10004), B.SSD_ERR_INVALID_ARG),
+    (dict(dstate=6), B.SSD_ERR_INVALID_ARG),
+    (dict(dstate=12), B.SSD_ERR_UNSUPPORTED),
+    (dict(num_slots=0), B.SSD_ERR_INVALID_ARG),
+])
+def test_decode_host_validation(lib, over, code):
+    a = _decode_args(**over)
+    assert lib.ssm_decode_update(ctypes.byref(a), None) == code
+
+
+def test_empty_decode_is_a_no_op(lib):
+    a = _decode_args(batch=0)
+    assert lib.ssm_decode_update(ctypes.byref(a), None) == B.SSD_OK
