@@ -32,10 +32,19 @@ import torch  # noqa: E402
 
 METRIC = "SSD prefill tokens/s/layer and decode state-updates/s; % HBM roofline on 1 GB300"
 UNIT = "tokens/s/layer"
-WORKLOAD = dict(workload="long-context mixed batch: 8 x 65536-token prefills + 384 single-token decodes",
-                num_prefills=8, prefill_len=65536, num_decodes=384, chunk_size=256, nheads=128,
-                headdim=64, dstate=128, ngroups=8, cache_slots=16384, token_dtype="bf16",
-                state_dtype="fp32", l2="inputs larger than L2 (no flush)")
+WORKLOADS = {
+    # the benchmark: every step of the path, long-context mixed batch
+    "long_mixed": dict(workload="long-context mixed batch: 8 x 65536-token prefills + 384 single-token decodes",
+                       num_prefills=8, prefill_len=65536, num_decodes=384, chunk_size=256, nheads=128,
+                       headdim=64, dstate=128, ngroups=8, cache_slots=16384, token_dtype="bf16",
+                       state_dtype="fp32", l2="inputs larger than L2 (no flush)"),
+    # a smaller case of the same kernels for profiler captures (about 4 GB on the device)
+    "prefill_8x8192": dict(workload="8 x 8192-token prefills (profiling size)", num_prefills=8, prefill_len=8192,
+                           num_decodes=0, chunk_size=256, nheads=128, headdim=64, dstate=128, ngroups=8,
+                           cache_slots=512, token_dtype="bf16", state_dtype="fp32",
+                           l2="inputs larger than L2 (no flush)"),
+}
+WORKLOAD = WORKLOADS["long_mixed"]
 
 
 def _peaks():
@@ -129,12 +138,13 @@ class ClockSampler:
 class Step:
     """Holds one rank's device-resident workload and runs the step."""
 
-    def __init__(self, dev):
+    def __init__(self, dev, wl):
         import selective_state_space_mamba2_gb300 as ssd
         from selective_state_space_mamba2_gb300 import workloads as W
         self.ssd = ssd
         self.dev = dev
-        self.pre, self.dec = W.long_mixed(dev)
+        self.pre, self.dec = W.long_mixed(dev, num_prefills=wl["num_prefills"], prefill_len=wl["prefill_len"],
+                                          num_decodes=wl["num_decodes"], num_slots=wl["cache_slots"])
         p = self.pre
         self.H, self.P = p["x"].shape[1], p["x"].shape[2]
         self.G, self.N = p["B"].shape[1], p["B"].shape[2]
@@ -179,8 +189,10 @@ class Step:
                                     chunk_size=p["chunk_size"], workspace=self.workspace)
         if ev is not None:
             ev[1].record()
-        self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
-                                   out=self.yd, D=d["D"], dt_bias=d["dt_bias"], null_block_id=d["null_block_id"])
+        if self.dec["live"] > 0:
+            self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
+                                       out=self.yd, D=d["D"], dt_bias=d["dt_bias"],
+                                       null_block_id=d["null_block_id"])
         if ev is not None:
             ev[2].record()
         if host is not None:
@@ -221,7 +233,8 @@ def gpu_arm(args, rank, world, dist_on):
     torch.cuda.set_device(dev)
     import selective_state_space_mamba2_gb300 as ssd
     ssd.build()
-    st = Step(dev)
+    wl = WORKLOADS[args.workload]
+    st = Step(dev, wl)
     H, P, N, G = st.H, st.P, st.N, st.G
     T = int(st.pre["cu_seqlens"][-1])
     R = st.dec["live"]
@@ -248,18 +261,20 @@ def gpu_arm(args, rank, world, dist_on):
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
 
     # end to end: inputs from pinned host memory, y back to host, every step
-    host, h2d, d2h = st.host_buffers()
-    st.run(host=host)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    _barrier(dist_on)
-    e0.record()
-    for _ in range(args.steps):
+    e2e_ms, h2d, d2h = None, 0, 0
+    if not args.no_e2e:
+        host, h2d, d2h = st.host_buffers()
         st.run(host=host)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_ms = _max_over_ranks(e0.elapsed_time(e1), dist_on, dev)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        _barrier(dist_on)
+        e0.record()
+        for _ in range(args.steps):
+            st.run(host=host)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = _max_over_ranks(e0.elapsed_time(e1), dist_on, dev)
 
     if rank != 0:
         return None
@@ -267,27 +282,28 @@ def gpu_arm(args, rank, world, dist_on):
     units = (T + R) * world
     hbm, peak_kind = _peaks()
     pre_mean = statistics.mean(pre_ms)
+    dec_mean = statistics.mean(dec_ms) if R > 0 else 0.0
     achieved = pre_bytes / (pre_mean * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": units / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded randn tokens, -exp(U(0,2)) A, U(-4,-1) dt_bias)",
-        "config": dict(WORKLOAD, parallelism="dp%d (independent replicas)" % world),
+        "config": dict(wl, parallelism="dp%d (independent replicas)" % world),
         "prefill": {"tokens_per_s_per_layer": T / (pre_mean * 1e-3), "ms": pre_mean,
                     "algorithmic_bytes": pre_bytes,
                     "hbm_frac": achieved / hbm},
-        "decode": {"state_updates_per_s": R / (statistics.mean(dec_ms) * 1e-3), "ms": statistics.mean(dec_ms),
+        "decode": {"state_updates_per_s": R / (dec_mean * 1e-3) if R else None, "ms": dec_mean,
                    "algorithmic_bytes": dec_bytes,
-                   "hbm_frac": dec_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9 / hbm},
+                   "hbm_frac": dec_bytes / (dec_mean * 1e-3) / 1e9 / hbm if R else None},
         "roofline": {"kernel": "ssd_prefill_varlen (%d kernels)" % st.prefill_kernels, "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": peak_kind, "traffic": None,
                      "units": "prefill algorithmic bytes per call / mean call time (CUDA events)"},
         "clocks": clk.summary(),
-        "e2e": {"value": units / (e2e_ms / args.steps * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": (st.prefill_kernels + 1) * args.steps,
+        "e2e": None if e2e_ms is None else {"value": units / (e2e_ms / args.steps * 1e-3), "unit": UNIT,
+                                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": (st.prefill_kernels + (1 if R else 0)) * args.steps,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -364,6 +380,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", default="long_mixed", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiler runs)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

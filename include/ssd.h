@@ -72,6 +72,7 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype_t;
 #define SSD_DEVERR_METADATA 0x2u /* chunk metadata inconsistent with cu_seqlens */
 #define SSD_DEVERR_COLUMN 0x4u   /* num_accepted_tokens outside [0, state_indices_cols) */
 #define SSD_DEVERR_TIMEOUT 0x8u  /* a bounded device-side wait gave up */
+#define SSD_DEVERR_INTERNAL 0x10u /* launch configuration not as the kernel requires (bug) */
 
 /* Human-readable name of a status code (static string). */
 SSD_API const char *ssd_status_string(ssd_status_t status);

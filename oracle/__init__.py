@@ -258,7 +258,7 @@ def ssm_decode(x, dt, A, B, C, read_states, live, D=None, dt_bias=None, dt_softp
     T, H, P = x.shape
     tpr = T // R
     assert tpr * R == T
-    N = np.asarray(B).shape[2]
+    N = _f64(B).shape[2]
     cu = np.arange(0, T + 1, tpr, dtype=np.int32)
     cc = np.arange(0, T + 1, dtype=np.int32)
     y, cs, _ = ssd_prefill(x, dt, A, B, C, cu, cc, D=D, dt_bias=dt_bias,

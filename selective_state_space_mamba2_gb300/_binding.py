@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libssd_gb300.so")
 
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE, SSD_ERR_CUDA = range(5)
 SSD_F32, SSD_BF16 = 0, 1
-DEVERR_SLOT, DEVERR_METADATA, DEVERR_COLUMN, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_SLOT, DEVERR_METADATA, DEVERR_COLUMN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8, 16
 
 EXPORTED_SYMBOLS = ("ssd_status_string", "ssd_abi_version", "ssd_max_chunks", "ssd_chunk_metadata",
                     "ssd_prefill_workspace_size", "ssd_prefill_kernel_count", "ssd_prefill_varlen",

@@ -62,6 +62,9 @@ cudaError_t simt_prefill_launch(const ssd_prefill_args &a, const PrefillWorkspac
                                 cudaStream_t s);
 bool simt_prefill_supported(const ssd_prefill_args &a);
 
+bool tc_prefill_supported(const ssd_prefill_args &a);
+cudaError_t tc_prefill_launch(const ssd_prefill_args &a, cudaStream_t s);
+
 bool decode_supported(const ssm_decode_args &a);
 cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s);
 }  // namespace ssd

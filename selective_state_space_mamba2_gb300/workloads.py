@@ -196,8 +196,8 @@ def long_mixed(device="cpu", seed=4, num_prefills=8, prefill_len=65536, num_deco
     free = [s for s in torch.randperm(num_slots - 1, generator=gcpu).add(1).tolist()
             if s not in used]
     assert len(free) >= num_decodes
-    si = torch.tensor(free[:num_decodes], dtype=torch.int32).view(num_decodes, 1)
-    x, dt, B, C = tokens(num_decodes, H, P, N, G, torch.bfloat16, device, seed + 1)
+    si = torch.tensor(free[:max(num_decodes, 1)], dtype=torch.int32).view(max(num_decodes, 1), 1)
+    x, dt, B, C = tokens(max(num_decodes, 1), H, P, N, G, torch.bfloat16, device, seed + 1)
     gi = _gen(device, seed + 32452843)
     cache = pre["cache"]
     for r in range(num_decodes):

@@ -25,6 +25,27 @@ def rel_err(a, b):
     return float(np.max(np.abs(a - b))) / max(rms, 1e-30)
 
 
+def where_worst(got, want, meta=None):
+    """Short description of where |got - want| is largest (for failure messages)."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    d = np.abs(got - want)
+    idx = np.unravel_index(int(np.argmax(d)), d.shape)
+    msg = "max at %s: got %.4g want %.4g" % (tuple(int(i) for i in idx), got[idx], want[idx])
+    if d.ndim == 3:  # [T, H, P]: worst tokens and heads
+        per_t = d.max(axis=(1, 2))
+        bad_t = np.nonzero(per_t > 0.02 * max(np.sqrt(np.mean(want * want)), 1e-30))[0]
+        msg += "; %d bad tokens %s" % (len(bad_t), bad_t[:12].tolist())
+        per_h = d.max(axis=(0, 2))
+        msg += "; per-head max %s" % np.round(per_h, 3).tolist()[:8]
+        if meta is not None and len(bad_t):
+            cc = np.asarray(meta["cu_chunk_seqlens"])
+            ks = np.searchsorted(cc, bad_t, side="right") - 1
+            msg += "; chunks %s offsets %s" % (sorted(set(ks.tolist()))[:8],
+                                               sorted(set((bad_t - cc[ks]).tolist()))[:12])
+    return msg
+
+
 def prefill_metadata(case):
     return ssd.ssd_chunk_metadata(case["cu_seqlens"], case["chunk_size"], case["num_computed"],
                                   case["has_init"], block_table=case["block_table"],
@@ -100,6 +121,8 @@ def check_prefill(case, y_gpu, meta, cache_before, cache_after, heads=None, **ok
     hs = slice(None) if heads is None else torch.tensor(heads)
     yg = y_gpu[:, hs].double().cpu().numpy()
     e_y = rel_err(yg, yo)
+    if e_y > tol:
+        print("y mismatch:", where_worst(yg, yo, meta))
     null = case["null_block_id"]
     written = [(k, int(s)) for k, s in enumerate(meta["chunk_slot"]) if int(s) != null]
     e_s = 0.0
