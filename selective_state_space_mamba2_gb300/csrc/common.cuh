@@ -53,7 +53,8 @@ __device__ __forceinline__ bool slot_usable(int32_t slot, int32_t null_id, int32
 namespace ssd {
 struct PrefillWorkspace {
     float *delta;        // [H, T]
-    float *cumlog;       // [H, T] inclusive in-chunk cumsum of delta * A
+    double *cumlog;      // [H, T] inclusive in-chunk cumsum of delta * A (fp64: decays are
+                         // exponentials of its differences)
     float *chunk_state;  // [K, H, P, N]
     float *state_in;     // [K, H, P, N]
 };

@@ -13,7 +13,9 @@
 //   4. chunk scan  y_t = sum_{s<=t} exp(c_t - c_s) delta_s (C_t.B_s) x_s
 //                        + exp(c_t) C_t . state_in + D x_t
 // Decays are always formed as exp of a non-positive difference c_t - c_s
-// (s <= t), never as a ratio of exponentials, so they cannot overflow.
+// (s <= t), never as a ratio of exponentials, so they cannot overflow.  The
+// cumsums are kept in fp64 and differenced there before an accurate expf, so
+// the fp32 path's decays carry no cancellation error from large |c|.
 #include "common.cuh"
 
 namespace ssd {
@@ -48,17 +50,18 @@ __global__ void __launch_bounds__(kThreads) cumsum_kernel(const ssd_prefill_args
     const float A = a.A[h];
     const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
     const size_t row = (size_t)h * a.total_tokens;
-    float carry = 0.f;
+    double carry = 0.0;
     for (int base = t0; base < t1; base += 32) {
         const int t = base + lane;
-        float d = 0.f, c = 0.f;
+        float d = 0.f;
+        double c = 0.0;
         if (t < t1) {
             d = step_delta(ldg_f32(dt + (size_t)t * a.nheads + h) + bias, a.dt_softplus, a.dt_min, a.dt_max);
-            c = d * A;
+            c = (double)d * (double)A;
         }
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const float v = __shfl_up_sync(0xffffffffu, c, off);
+            const double v = __shfl_up_sync(0xffffffffu, c, off);
             if (lane >= off) c += v;
         }
         c += carry;
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ssd_prefill
     const Tin *x = static_cast<const Tin *>(a.x);
     const Tin *B = static_cast<const Tin *>(a.B);
     const size_t hrow = (size_t)h * a.total_tokens;
-    const float c_end = t1 > t0 ? ws.cumlog[hrow + t1 - 1] : 0.f;
+    const double c_end = t1 > t0 ? ws.cumlog[hrow + t1 - 1] : 0.0;
 
     float acc[OPT];
     int pofs[OPT], nofs[OPT];
@@ -111,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) chunk_state_kernel(const ssd_prefill
         }
         if (threadIdx.x < kStateTile) {
             const int t = base + threadIdx.x;
-            sw[threadIdx.x] = t < t1 ? __expf(c_end - ws.cumlog[hrow + t]) * ws.delta[hrow + t] : 0.f;
+            sw[threadIdx.x] = t < t1 ? expf((float)(c_end - ws.cumlog[hrow + t])) * ws.delta[hrow + t] : 0.f;
         }
         __syncthreads();
 #pragma unroll 4
@@ -160,8 +163,8 @@ __global__ void __launch_bounds__(kThreads) state_pass_kernel(const ssd_prefill_
             return;
         }
         ws.state_in[(size_t)k * H * PN + head_off] = s;
-        const float c_end = ws.cumlog[hrow + t1 - 1];
-        s = fmaf(__expf(c_end), s, ws.chunk_state[(size_t)k * H * PN + head_off]);
+        const float decay = (float)exp(ws.cumlog[hrow + t1 - 1]);
+        s = fmaf(decay, s, ws.chunk_state[(size_t)k * H * PN + head_off]);
         const int32_t cs = a.chunk_slot ? a.chunk_slot[k] : a.null_block_id;
         if (slot_usable(cs, a.null_block_id, a.num_slots, reporter ? a.err_word : nullptr))
             a.state_cache[(size_t)cs * H * PN + head_off] = s;
@@ -171,6 +174,14 @@ __global__ void __launch_bounds__(kThreads) state_pass_kernel(const ssd_prefill_
 // ---------------------------------------------------------------- step 4 ----
 constexpr int kScanRows = 32;  // output tokens per CTA
 constexpr int kScanCols = 32;  // source tokens per round
+
+// floats in front of the two fp64 vectors of the scan kernel, rounded up to an
+// even count so the fp64 part is 8-byte aligned
+__host__ __device__ __forceinline__ size_t scan_float_slots(int P, int N) {
+    const size_t nf = (size_t)P * (N + 1) + kScanRows * N + kScanCols * (N + 1) + kScanCols * P +
+                      kScanRows * (kScanCols + 1) + kScanCols;
+    return (nf + 1) & ~(size_t)1;
+}
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_args a, PrefillWorkspace ws) {
@@ -186,9 +197,9 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_
     float *sB = sC + kScanRows * N;           // [cols][N+1] (padded: column reads stride by row)
     float *sx = sB + kScanCols * Ns;          // [cols][P]
     float *sM = sx + kScanCols * P;           // [rows][cols+1]
-    float *scr = sM + kScanRows * (kScanCols + 1);  // [rows] c_t
-    float *scs = scr + kScanRows;             // [cols] c_s
-    float *sds = scs + kScanCols;             // [cols] delta_s
+    float *sds = sM + kScanRows * (kScanCols + 1);  // [cols] delta_s
+    double *scr = reinterpret_cast<double *>(smem + scan_float_slots(P, N));  // [rows] c_t (8-byte aligned)
+    double *scs = scr + kScanRows;            // [cols] c_s
 
     const Tin *x = static_cast<const Tin *>(a.x);
     const Tin *B = static_cast<const Tin *>(a.B);
@@ -217,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_
         }
         if (threadIdx.x < kScanRows) {
             const int t = ta + threadIdx.x;
-            scr[threadIdx.x] = t < tb ? ws.cumlog[hrow + t] : 0.f;
+            scr[threadIdx.x] = t < tb ? ws.cumlog[hrow + t] : 0.0;
         }
         __syncthreads();
         float acc[kScanRows];
@@ -233,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_
             }
 #pragma unroll
             for (int i = 0; i < kScanRows; ++i)
-                if (my_r0 + i * row_groups < kScanRows) acc[i] *= __expf(scr[my_r0 + i * row_groups]);
+                if (my_r0 + i * row_groups < kScanRows) acc[i] *= (float)exp(scr[my_r0 + i * row_groups]);
         }
         // in-chunk contributions from source tokens s in [t0, tb)
         for (int sa = t0; sa < tb; sa += kScanCols) {
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_
             }
             if (threadIdx.x < kScanCols) {
                 const int s = sa + threadIdx.x;
-                scs[threadIdx.x] = s < tb ? ws.cumlog[hrow + s] : 0.f;
+                scs[threadIdx.x] = s < tb ? ws.cumlog[hrow + s] : 0.0;
                 sds[threadIdx.x] = s < tb ? ws.delta[hrow + s] : 0.f;
             }
             __syncthreads();
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_
                 if (t < tb && s <= t) {
                     float dot = 0.f;
                     for (int n = 0; n < N; ++n) dot = fmaf(sC[rr * N + n], sB[cc * Ns + n], dot);
-                    m = dot * __expf(scr[rr] - scs[cc]) * sds[cc];
+                    m = dot * expf((float)(scr[rr] - scs[cc])) * sds[cc];
                 }
                 sM[rr * (kScanCols + 1) + cc] = m;
             }
@@ -291,8 +302,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_
 
 size_t scan_smem_bytes(const ssd_prefill_args &a) {
     const int P = a.headdim, N = a.dstate;
-    return sizeof(float) * ((size_t)P * (N + 1) + kScanRows * N + kScanCols * (N + 1) + kScanCols * P +
-                            kScanRows * (kScanCols + 1) + kScanRows + 2 * kScanCols);
+    return sizeof(float) * scan_float_slots(P, N) + sizeof(double) * (kScanRows + kScanCols);
 }
 
 size_t state_smem_bytes(const ssd_prefill_args &a) {
@@ -344,15 +354,16 @@ bool simt_prefill_supported(const ssd_prefill_args &a) {
 
 size_t simt_prefill_workspace(const ssd_prefill_args &a, PrefillWorkspace *ws, void *base) {
     const size_t per_tok = align_up(sizeof(float) * (size_t)a.nheads * a.total_tokens);
+    const size_t per_tok64 = align_up(sizeof(double) * (size_t)a.nheads * a.total_tokens);
     const size_t per_chunk = align_up(sizeof(float) * (size_t)a.num_chunks * a.nheads * a.headdim * a.dstate);
     if (ws) {
         char *p = static_cast<char *>(base);
         ws->delta = reinterpret_cast<float *>(p);
-        ws->cumlog = reinterpret_cast<float *>(p + per_tok);
-        ws->chunk_state = reinterpret_cast<float *>(p + 2 * per_tok);
-        ws->state_in = reinterpret_cast<float *>(p + 2 * per_tok + per_chunk);
+        ws->cumlog = reinterpret_cast<double *>(p + per_tok);
+        ws->chunk_state = reinterpret_cast<float *>(p + per_tok + per_tok64);
+        ws->state_in = reinterpret_cast<float *>(p + per_tok + per_tok64 + per_chunk);
     }
-    return 2 * per_tok + 2 * per_chunk;
+    return per_tok + per_tok64 + 2 * per_chunk;
 }
 
 cudaError_t simt_prefill_launch(const ssd_prefill_args &a, const PrefillWorkspace &ws, cudaStream_t s) {

@@ -9,7 +9,12 @@
 // 프리픽스 캐싱" on "[vLLM] Mamba (SSM): 선형 시간 복잡도 시퀀스 모델링").
 //
 // Per block of L <= 128 tokens [tb, tb+L) with in-block cumsum c_t of
-// delta*A, the four dense contractions run as tcgen05.mma tiles:
+// delta*A, the four dense contractions run as tcgen05.mma tiles (fp32
+// accumulators).  M1 takes the bf16 inputs as they are; the operands the
+// kernel forms itself (P, w x, the carried state) are rounded to fp16, whose
+// 11-bit significand keeps their rounding error 8x below bf16's, and the x, B
+// and C tiles they meet are converted to fp16 in shared memory (exactly, for
+// values in fp16's range) because both operands of an MMA share one type:
 //   M1  S  = C B^T                  [128 x 128], K = dstate   (SS, K/K-major)
 //   M2  Y1 = P X                    [128 x  64], K = tokens   (TS: P in TMEM)
 //        P[t,s] = exp(c_t - c_s) delta_s S[t,s] for s <= t, plus D on the diagonal
@@ -115,16 +120,28 @@ struct Cursor {
     }
 };
 
-// bf16 copy of the state row (dstate row n = thread) into the M3 operand tile
+// fp16 copy of the state row (dstate row n = thread) into the M3 operand tile
 __device__ __forceinline__ void store_state_row(uint8_t *sH, int n, const float (&st)[kP]) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         uint4 v;
-        v.x = pack_bf16(st[8 * c + 0], st[8 * c + 1]);
-        v.y = pack_bf16(st[8 * c + 2], st[8 * c + 3]);
-        v.z = pack_bf16(st[8 * c + 4], st[8 * c + 5]);
-        v.w = pack_bf16(st[8 * c + 6], st[8 * c + 7]);
+        v.x = pack_f16_sat(st[8 * c + 0], st[8 * c + 1]);
+        v.y = pack_f16_sat(st[8 * c + 2], st[8 * c + 3]);
+        v.z = pack_f16_sat(st[8 * c + 4], st[8 * c + 5]);
+        v.w = pack_f16_sat(st[8 * c + 6], st[8 * c + 7]);
         *reinterpret_cast<uint4 *>(sH + sw128_offset(n, c)) = v;
+    }
+}
+
+// row r of a [128 x 128] bf16 tile held as two 64-wide swizzled atoms -> fp16, in place
+__device__ __forceinline__ void tile_row_to_f16(uint8_t *tile, int r) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint4 *q = reinterpret_cast<uint4 *>(tile + a * 16384 + sw128_offset(r, c));
+            *q = bf16x8_to_f16x8(*q);
+        }
     }
 }
 
@@ -213,9 +230,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             const uint32_t aC = smem_u32(sC), aB = smem_u32(sB), aX = smem_u32(sX), aXW = smem_u32(sXW),
                            aH = smem_u32(sH);
-            constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);
-            constexpr uint32_t kIdY = idesc_bf16(128, 64, 0, 1);
-            constexpr uint32_t kIdD = idesc_bf16(128, 64, 1, 1);
+            constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // raw bf16 C and B
+            constexpr uint32_t kIdY = idesc_f16(128, 64, 0, 1);    // fp16 operands from here on
+            constexpr uint32_t kIdD = idesc_f16(128, 64, 1, 1);
             int committed = 0;  // blocks whose final commit was issued
             for (int i = 0; i < nblocks; ++i) {
                 const uint32_t ph = i & 1;
@@ -321,16 +338,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             {
-                const __nv_bfloat162 w2 = __float2bfloat162_rn(w_x);
+                // x row t: w x into the M4 operand (fp16) and x itself -> fp16 in place (M2 operand)
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
                     uint4 v = *reinterpret_cast<const uint4 *>(sX + sw128_offset(t, cc));
-                    __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
-                    e[0] = __hmul2(e[0], w2);
-                    e[1] = __hmul2(e[1], w2);
-                    e[2] = __hmul2(e[2], w2);
-                    e[3] = __hmul2(e[3], w2);
-                    *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = v;
+                    uint4 xw;
+                    xw.x = pack_f16_sat(w_x * __uint_as_float(v.x << 16), w_x * __uint_as_float(v.x & 0xFFFF0000u));
+                    xw.y = pack_f16_sat(w_x * __uint_as_float(v.y << 16), w_x * __uint_as_float(v.y & 0xFFFF0000u));
+                    xw.z = pack_f16_sat(w_x * __uint_as_float(v.z << 16), w_x * __uint_as_float(v.z & 0xFFFF0000u));
+                    xw.w = pack_f16_sat(w_x * __uint_as_float(v.w << 16), w_x * __uint_as_float(v.w & 0xFFFF0000u));
+                    *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
+                    *reinterpret_cast<uint4 *>(sX + sw128_offset(t, cc)) = bf16x8_to_f16x8(v);
                 }
             }
             // ---- S ready: P pass, S (fp32) -> P (bf16) in TMEM
@@ -355,9 +373,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 f = f4[q];
-                        pk[2 * q] = pack_bf16(__uint_as_float(v[4 * q]) * f.x * R, __uint_as_float(v[4 * q + 1]) * f.y * R);
-                        pk[2 * q + 1] =
-                            pack_bf16(__uint_as_float(v[4 * q + 2]) * f.z * R, __uint_as_float(v[4 * q + 3]) * f.w * R);
+                        pk[2 * q] = pack_f16_sat(__uint_as_float(v[4 * q]) * f.x * R, __uint_as_float(v[4 * q + 1]) * f.y * R);
+                        pk[2 * q + 1] = pack_f16_sat(__uint_as_float(v[4 * q + 2]) * f.z * R,
+                                                     __uint_as_float(v[4 * q + 3]) * f.w * R);
                     }
                 } else if (j == warp) {
                     uint32_t v[32];
@@ -373,15 +391,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                         pv[q] = val;
                     }
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) pk[q] = pack_bf16(pv[2 * q], pv[2 * q + 1]);
+                    for (int q = 0; q < 16; ++q) pk[q] = pack_f16_sat(pv[2 * q], pv[2 * q + 1]);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 16; ++q) pk[q] = 0u;
                 }
                 tmem_st16(tm + lane_base + COL_P + 16 * j, pk);
             }
+            // M1 is done with the raw tiles: C and B rows -> fp16 for M3 and M4
+            tile_row_to_f16(sC, t);
+            tile_row_to_f16(sB, t);
             tmem_st_wait();
-            fence_proxy_async_smem();  // w x and the state tile -> async proxy
+            fence_proxy_async_smem();  // w x, x, B, C and the state tile -> async proxy
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[BAR_P]);

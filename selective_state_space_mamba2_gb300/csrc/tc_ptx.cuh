@@ -159,6 +159,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32
            | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Same with fp16 A and B (formats 0).
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t a_mn_major, uint32_t b_mn_major) {
+    return (1u << 4) | (a_mn_major << 15) | (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -189,6 +194,23 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// fp16 pair, saturating to the finite range (lo in the low half)
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 8 bf16 (a 16-byte chunk) -> 8 fp16, in the same order
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    uint4 o;
+    o.x = pack_f16_sat(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
+    o.y = pack_f16_sat(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+    o.z = pack_f16_sat(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
+    o.w = pack_f16_sat(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+    return o;
 }
 
 // byte offset of 16-byte chunk `c` of row `r` in a 128-byte-swizzled tile

@@ -2,8 +2,14 @@
 with the CPU oracle on the same (bf16-rounded) inputs.
 
 Tolerance, as a ratio max|gpu - oracle| / RMS(oracle) over the compared
-elements: 2e-2 for bf16 inputs and 1e-4 for fp32 inputs.  Slot ids, chunk
-metadata and slots the call must not touch are compared bit for bit.
+elements: 2e-2 for bf16 inputs and 1e-4 for fp32 inputs.  States are fp32
+and are compared that way.  y is stored in the input dtype; for bf16 that
+storage alone moves a value by up to half a bf16 ulp, which for these
+heavy-tailed outputs (max|y| / RMS(y) reaches 40) exceeds 2e-2 of the RMS
+even for the exactly rounded oracle.  So for bf16 y the error counted is the
+part beyond half an ulp at the element's magnitude: it bounds the error of
+the value the kernel computed before it was stored.  Slot ids, chunk metadata
+and slots the call must not touch are compared bit for bit.
 """
 import math
 
@@ -23,6 +29,26 @@ def rel_err(a, b):
         return 0.0
     rms = math.sqrt(float(np.mean(b * b)))
     return float(np.max(np.abs(a - b))) / max(rms, 1e-30)
+
+
+def ulp_bf16(v):
+    """Spacing of bf16 numbers at magnitude |v| (8 significant bits)."""
+    a = np.maximum(np.abs(np.asarray(v, np.float64)), 1.1754943508222875e-38)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+def y_err(got, want, dtype):
+    """max error / RMS(want); for bf16 outputs the first half ulp is excused."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    if got.size == 0:
+        return 0.0
+    if dtype != torch.bfloat16:
+        return rel_err(got, want)
+    allow = 0.5 * ulp_bf16(np.maximum(np.abs(got), np.abs(want)))
+    excess = np.maximum(np.abs(got - want) - allow, 0.0)
+    rms = math.sqrt(float(np.mean(want * want)))
+    return float(excess.max()) / max(rms, 1e-30)
 
 
 def where_worst(got, want, meta=None):
@@ -120,7 +146,7 @@ def check_prefill(case, y_gpu, meta, cache_before, cache_after, heads=None, **ok
     yo, cso = oracle_prefill(case, meta, cache_before, heads=heads, **okw)
     hs = slice(None) if heads is None else torch.tensor(heads)
     yg = y_gpu[:, hs].double().cpu().numpy()
-    e_y = rel_err(yg, yo)
+    e_y = y_err(yg, yo, case["x"].dtype)
     if e_y > tol:
         print("y mismatch:", where_worst(yg, yo, meta))
     null = case["null_block_id"]
@@ -131,6 +157,8 @@ def check_prefill(case, y_gpu, meta, cache_before, cache_after, heads=None, **ok
         sl = torch.tensor([s for _, s in written], device=cache_after.device)
         got = cache_after[sl][:, hs].double().cpu().numpy()
         e_s = rel_err(got, cso[ks])
+        if e_s > tol:
+            print("state mismatch:", where_worst(got, cso[ks]))
     # untouched slots: bitwise
     mask = torch.ones(cache_after.shape[0], dtype=torch.bool, device=cache_after.device)
     if written:
@@ -175,7 +203,7 @@ def check_decode(case, y_gpu, cache_before, cache_after, requests=None, check_un
                                dt_bias=case["dt_bias"].cpu())
     yg = y_gpu[rows].double().cpu().numpy()
     liverows = np.array([rd[r] != null for r in req for _ in range(tpr)])
-    e_y = rel_err(yg[liverows], yo[liverows])
+    e_y = y_err(yg[liverows], yo[liverows], case["x"].dtype)
     dead_ok = bool(np.all(np.isnan(yg[~liverows]))) if (~liverows).any() else True
     got, want = [], []
     for i, r in enumerate(req):
