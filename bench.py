@@ -157,7 +157,7 @@ class Step:
         m = self.device_meta(self.meta)
         a = ssd.prefill_args(p["x"], p["dt"], p["A"], p["B"], p["C"], self.cu_dev, m["cu_chunk_seqlens"],
                              m["seq_idx"], m["last_chunk_indices"], self.y, m["init_slot"], m["chunk_slot"],
-                             p["cache"], p["D"], p["dt_bias"], chunk_size=p["chunk_size"])
+                             p["cache"], p["D"], p["dt_bias"], chunk_size=p["chunk_size"], seq_order=m["seq_order"])
         self.workspace = torch.empty(max(ssd.ssd_prefill_workspace_size(a), 1), dtype=torch.uint8, device=dev)
         self.prefill_kernels = ssd.ssd_prefill_kernel_count(a)
         self.stream = torch.cuda.current_stream()
@@ -186,7 +186,7 @@ class Step:
                                     m["seq_idx"], m["last_chunk_indices"], out=self.y, init_slot=m["init_slot"],
                                     chunk_slot=m["chunk_slot"], state_cache=p["cache"], D=p["D"],
                                     dt_bias=p["dt_bias"], null_block_id=p["null_block_id"],
-                                    chunk_size=p["chunk_size"], workspace=self.workspace)
+                                    chunk_size=p["chunk_size"], workspace=self.workspace, seq_order=m["seq_order"])
         if ev is not None:
             ev[1].record()
         if self.dec["live"] > 0:

@@ -130,6 +130,9 @@ SSD_API int32_t ssd_max_chunks(int32_t num_seqs, int32_t total_tokens, int32_t c
  *                              null_block_id (may be NULL).  "all" mode:
  *                              block_table[seq, chunk_block_col]; default mode:
  *                              state_indices[seq] for the sequence's last chunk.
+ *   seq_order           [S]    sequences by decreasing number of new tokens (ties in
+ *                              index order), or NULL; pass it as ssd_prefill_args.seq_order
+ *                              so the longest sequences start first.
  *   num_chunks_out             K.
  * Errors: SSD_ERR_INVALID_ARG for bad sizes, a decreasing cu_seqlens, negative
  * num_computed_tokens, has_initial_states with num_computed_tokens == 0 in
@@ -143,7 +146,8 @@ SSD_API ssd_status_t ssd_chunk_metadata(int32_t num_seqs, int32_t chunk_size, co
                                 const int32_t *state_indices, int32_t null_block_id,
                                 int32_t max_chunks, int32_t *cu_chunk_seqlens, int32_t *seq_idx,
                                 int32_t *last_chunk_indices, int32_t *chunk_block_col,
-                                int32_t *init_slot, int32_t *chunk_slot, int32_t *num_chunks_out);
+                                int32_t *init_slot, int32_t *chunk_slot, int32_t *seq_order,
+                                int32_t *num_chunks_out);
 
 /* ------------------------------------------------------------------------ *
  * Varlen SSD prefill (device)
@@ -188,6 +192,9 @@ typedef struct ssd_prefill_args {
                                   when init_slot and chunk_slot are both NULL */
     void *y;                   /* [T, H, P] dtype, 16-byte aligned, written for every token */
     uint32_t *err_word;        /* device word or NULL */
+    const int32_t *seq_order;  /* [S] device, a permutation of 0..S-1 giving the order in which
+                                  sequences are started (longest first balances the GPU), or
+                                  NULL for index order; results do not depend on it */
 } ssd_prefill_args;
 
 /* Bytes of device workspace ssd_prefill_varlen needs for these arguments

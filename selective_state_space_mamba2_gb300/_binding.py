@@ -37,7 +37,7 @@ class PrefillArgs(ctypes.Structure):
                 ("x", _vp), ("dt", _vp), ("B", _vp), ("C", _vp), ("z", _vp), ("A", _vp), ("D", _vp),
                 ("dt_bias", _vp), ("cu_seqlens", _vp), ("cu_chunk_seqlens", _vp), ("seq_idx", _vp),
                 ("last_chunk_indices", _vp), ("init_slot", _vp), ("chunk_slot", _vp),
-                ("state_cache", _vp), ("y", _vp), ("err_word", _vp)]
+                ("state_cache", _vp), ("y", _vp), ("err_word", _vp), ("seq_order", _vp)]
 
 
 class DecodeArgs(ctypes.Structure):
@@ -78,7 +78,7 @@ def lib():
         L.ssd_chunk_metadata.restype = ctypes.c_int
         L.ssd_chunk_metadata.argtypes = [_i32, _i32, ip, ip, ctypes.POINTER(ctypes.c_uint8), ip,
                                          ctypes.c_int64, _i32, ip, _i32, _i32, ip, ip, ip, ip, ip,
-                                         ip, ip]
+                                         ip, ip, ip]
         L.ssd_prefill_workspace_size.restype = ctypes.c_size_t
         L.ssd_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
         L.ssd_prefill_kernel_count.restype = _i32
@@ -147,7 +147,7 @@ def ssd_chunk_metadata(cu_seqlens, chunk_size, num_computed_tokens=None, has_ini
 
     All inputs are host arrays; returns a dict of int32 numpy arrays:
     cu_chunk_seqlens [K+1], seq_idx [K], last_chunk_indices [S],
-    chunk_block_col [K], init_slot [S], chunk_slot [K].
+    chunk_block_col [K], init_slot [S], chunk_slot [K], seq_order [S].
     """
     cu = _host_i32(cu_seqlens, "cu_seqlens")
     S = cu.shape[0] - 1
@@ -163,26 +163,27 @@ def ssd_chunk_metadata(cu_seqlens, chunk_size, num_computed_tokens=None, has_ini
     out = dict(cu_chunk_seqlens=np.zeros(maxk + 1, np.int32), seq_idx=np.zeros(max(maxk, 1), np.int32),
                last_chunk_indices=np.zeros(max(S, 1), np.int32),
                chunk_block_col=np.zeros(max(maxk, 1), np.int32), init_slot=np.zeros(max(S, 1), np.int32),
-               chunk_slot=np.zeros(max(maxk, 1), np.int32))
+               chunk_slot=np.zeros(max(maxk, 1), np.int32), seq_order=np.zeros(max(S, 1), np.int32))
     k = ctypes.c_int32(0)
     rc = lib().ssd_chunk_metadata(
         S, int(chunk_size), _ptr(cu), _ptr(nc), _ptr(has, ctypes.c_uint8), _ptr(bt),
         0 if bt is None else bt.shape[1], 0 if bt is None else bt.shape[1], _ptr(si), int(null_block_id),
         maxk, _ptr(out["cu_chunk_seqlens"]), _ptr(out["seq_idx"]), _ptr(out["last_chunk_indices"]),
-        _ptr(out["chunk_block_col"]), _ptr(out["init_slot"]), _ptr(out["chunk_slot"]), ctypes.byref(k))
+        _ptr(out["chunk_block_col"]), _ptr(out["init_slot"]), _ptr(out["chunk_slot"]), _ptr(out["seq_order"]),
+        ctypes.byref(k))
     if rc != SSD_OK:
         raise SSDError("ssd_chunk_metadata", rc)
     K = k.value
     return dict(cu_chunk_seqlens=out["cu_chunk_seqlens"][:K + 1].copy(), seq_idx=out["seq_idx"][:K].copy(),
                 last_chunk_indices=out["last_chunk_indices"][:S].copy(),
                 chunk_block_col=out["chunk_block_col"][:K].copy(), init_slot=out["init_slot"][:S].copy(),
-                chunk_slot=out["chunk_slot"][:K].copy())
+                chunk_slot=out["chunk_slot"][:K].copy(), seq_order=out["seq_order"][:S].copy())
 
 
 def prefill_args(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices, out,
                  init_slot=None, chunk_slot=None, state_cache=None, D=None, dt_bias=None, z=None,
                  dt_softplus=True, dt_limit=(0.0, math.inf), null_block_id=0, chunk_size=None,
-                 err_word=None):
+                 err_word=None, seq_order=None):
     """Fills a ``PrefillArgs`` from device tensors (validating shapes and dtypes)."""
     T, H, P = x.shape
     G, N = B.shape[1], B.shape[2]
@@ -217,6 +218,7 @@ def prefill_args(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chu
         a.state_cache = _dev(state_cache, "state_cache")
         a.num_slots = state_cache.shape[0]
     a.err_word = _dev(err_word, "err_word", required=False)
+    a.seq_order = _dev(seq_order, "seq_order", torch.int32, required=False)
     if a.chunk_size == 0:
         a.chunk_size = 1
     return a
@@ -233,7 +235,8 @@ def ssd_prefill_kernel_count(args):
 def ssd_prefill_varlen(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices,
                        out=None, init_slot=None, chunk_slot=None, state_cache=None, D=None,
                        dt_bias=None, z=None, dt_softplus=True, dt_limit=(0.0, math.inf),
-                       null_block_id=0, chunk_size=None, workspace=None, err_word=None, stream=None):
+                       null_block_id=0, chunk_size=None, workspace=None, err_word=None, stream=None,
+                       seq_order=None):
     """Varlen SSD prefill on device tensors; returns ``out`` ([T,H,P], x's dtype).
 
     ``workspace`` (uint8 CUDA tensor) is allocated with torch when omitted.
@@ -242,7 +245,7 @@ def ssd_prefill_varlen(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, la
         out = torch.empty_like(x)
     a = prefill_args(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices, out,
                      init_slot, chunk_slot, state_cache, D, dt_bias, z, dt_softplus, dt_limit,
-                     null_block_id, chunk_size, err_word)
+                     null_block_id, chunk_size, err_word, seq_order)
     need = ssd_prefill_workspace_size(a)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)

@@ -9,7 +9,10 @@
 // chunk_size block; default mode: one slot per request).
 //
 // O(S + K) work; pure and deterministic; runs on host memory only.
+#include <algorithm>
 #include <cstdint>
+#include <numeric>
+#include <vector>
 
 #include "ssd.h"
 
@@ -27,7 +30,8 @@ extern "C" ssd_status_t ssd_chunk_metadata(
     const int32_t *block_table, int64_t block_table_stride, int32_t block_table_cols,
     const int32_t *state_indices, int32_t null_block_id, int32_t max_chunks,
     int32_t *cu_chunk_seqlens, int32_t *seq_idx, int32_t *last_chunk_indices,
-    int32_t *chunk_block_col, int32_t *init_slot, int32_t *chunk_slot, int32_t *num_chunks_out) {
+    int32_t *chunk_block_col, int32_t *init_slot, int32_t *chunk_slot, int32_t *seq_order,
+    int32_t *num_chunks_out) {
     if (num_seqs < 0 || chunk_size < 1 || max_chunks < 0 || !cu_seqlens || !cu_chunk_seqlens ||
         !num_chunks_out || (num_seqs > 0 && (!seq_idx || !last_chunk_indices)))
         return SSD_ERR_INVALID_ARG;
@@ -106,6 +110,14 @@ extern "C" ssd_status_t ssd_chunk_metadata(
                 chunk_slot[c] = slot;
             }
         }
+    }
+    if (seq_order) {
+        std::vector<int32_t> idx(num_seqs);
+        std::iota(idx.begin(), idx.end(), 0);
+        std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
+            return cu_seqlens[a + 1] - cu_seqlens[a] > cu_seqlens[b + 1] - cu_seqlens[b];
+        });
+        std::copy(idx.begin(), idx.end(), seq_order);
     }
     *num_chunks_out = k;
     return SSD_OK;

@@ -54,6 +54,7 @@ struct TcParams {
     float *cache;
     __nv_bfloat16 *y;
     uint32_t *err;
+    const int32_t *seq_order;
 };
 
 namespace {
@@ -150,8 +151,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                           const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = blockIdx.x / p.H;
-    const int h = blockIdx.x - r * p.H;
+    const int slot_r = blockIdx.x / p.H;
+    const int h = blockIdx.x - slot_r * p.H;
+    const int r = p.seq_order ? p.seq_order[slot_r] : slot_r;
+    if (r < 0 || r >= p.S) {
+        if (threadIdx.x == 0 && h == 0) report(p.err, SSD_DEVERR_METADATA);
+        return;
+    }
     const int g = h / (p.H / p.G);
 
     // ---- the sequence's chunk range, validated before anything is set up
@@ -511,6 +517,7 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, cudaStream_t s) {
     p.cache = a.state_cache;
     p.y = static_cast<__nv_bfloat16 *>(a.y);
     p.err = a.err_word;
+    p.seq_order = a.seq_order;
     cudaError_t e = cudaFuncSetAttribute(ssd_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;

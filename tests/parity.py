@@ -89,7 +89,7 @@ def run_prefill(case, meta=None, err=None, **kw):
         t["cu_chunk_seqlens"], t["seq_idx"], t["last_chunk_indices"], init_slot=t["init_slot"],
         chunk_slot=t["chunk_slot"], state_cache=case["cache"], D=kw.pop("D", case["D"]),
         dt_bias=kw.pop("dt_bias", case["dt_bias"]), null_block_id=case["null_block_id"],
-        chunk_size=case["chunk_size"], err_word=err, **kw)
+        chunk_size=case["chunk_size"], err_word=err, seq_order=t.get("seq_order"), **kw)
     return y, meta
 
 

@@ -70,6 +70,12 @@ def test_metadata_matches_oracle_bit_exact(lib, oracle_lib, seed):
     assert np.array_equal(md["init_slot"], init_d) and np.array_equal(md["chunk_slot"], cslot_d)
 
 
+def test_seq_order_is_longest_first_permutation(lib):
+    cu = np.array([0, 5, 5, 30, 31, 40, 65], np.int32)  # lengths 5, 0, 25, 1, 9, 25
+    m = ssd.ssd_chunk_metadata(cu, 8)
+    assert m["seq_order"].tolist() == [2, 5, 4, 0, 3, 1]
+
+
 def test_metadata_rejects_bad_input(lib):
     with pytest.raises(B.SSDError) as e:
         ssd.ssd_chunk_metadata([0, 5, 3], 4)
