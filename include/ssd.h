@@ -217,6 +217,39 @@ SSD_API int32_t ssd_prefill_kernel_count(const ssd_prefill_args *args);
 SSD_API ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *args, void *workspace,
                                 size_t workspace_bytes, ssd_stream_t stream);
 
+/*
+ * ssd_prefill_varlen_noalloc -- the prefill for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call.  It exists for callers that
+ * cannot give the library device memory at call time: a serving engine that
+ * reserved all free device memory up front (for its state cache) and hands
+ * none out afterwards, or a host that only has this C ABI and no device
+ * allocator.  It runs the CUDA-core prefill (the kernels that need scratch
+ * memory; for every dtype and shape, including those ssd_prefill_varlen would
+ * send to the tensor-core kernel) with its scratch in one file-scope device
+ * array of SSD_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Arguments, results and host checks are those of ssd_prefill_varlen, minus
+ * the workspace.  The call needs up256(4*H*T) + up256(8*H*T) +
+ * 2*up256(4*K*H*P*N) bytes of scratch (up256 rounds up to a multiple of 256;
+ * e.g. about 4.3 MB for one 2048-token chunk with H=48, P=64, N=128) and
+ * returns SSD_ERR_WORKSPACE when that exceeds SSD_NOALLOC_SCRATCH_BYTES;
+ * SSD_ERR_UNSUPPORTED for shapes the CUDA-core path does not take.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and keeps it; make that first call before any stream
+ * capture.  All calls share the one array, and each call leaves its scratch
+ * contents behind; nothing in it needs to start at zero, because with
+ * metadata from ssd_chunk_metadata every value a call reads was written
+ * earlier in the same call.  Calls whose kernels
+ * overlap on the GPU (different streams, or different host threads without
+ * ordering) race on the array.
+ */
+#define SSD_NOALLOC_SCRATCH_BYTES (64u << 20)
+SSD_API ssd_status_t ssd_prefill_varlen_noalloc(const ssd_prefill_args *args, ssd_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Decode state update (device)
  *

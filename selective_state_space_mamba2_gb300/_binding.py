@@ -22,7 +22,7 @@ DEVERR_SLOT, DEVERR_METADATA, DEVERR_COLUMN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1
 
 EXPORTED_SYMBOLS = ("ssd_status_string", "ssd_abi_version", "ssd_max_chunks", "ssd_chunk_metadata",
                     "ssd_prefill_workspace_size", "ssd_prefill_kernel_count", "ssd_prefill_varlen",
-                    "ssm_decode_update")
+                    "ssd_prefill_varlen_noalloc", "ssm_decode_update")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -85,6 +85,8 @@ def lib():
         L.ssd_prefill_kernel_count.argtypes = [ctypes.POINTER(PrefillArgs)]
         L.ssd_prefill_varlen.restype = ctypes.c_int
         L.ssd_prefill_varlen.argtypes = [ctypes.POINTER(PrefillArgs), _vp, ctypes.c_size_t, _vp]
+        L.ssd_prefill_varlen_noalloc.restype = ctypes.c_int
+        L.ssd_prefill_varlen_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
         L.ssm_decode_update.restype = ctypes.c_int
         L.ssm_decode_update.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
         _lib = L

@@ -51,6 +51,21 @@ def y_err(got, want, dtype):
     return float(excess.max()) / max(rms, 1e-30)
 
 
+def y_err_pair(a, b, dtype):
+    """Like y_err, for two outputs of the GPU path: when both were rounded to
+    bf16, each rounding moves a value by up to half an ulp, so one ulp is
+    excused; normalised by RMS(b)."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    if a.size == 0:
+        return 0.0
+    if dtype != torch.bfloat16:
+        return rel_err(a, b)
+    allow = ulp_bf16(np.maximum(np.abs(a), np.abs(b)))
+    excess = np.maximum(np.abs(a - b) - allow, 0.0)
+    return float(excess.max()) / max(math.sqrt(float(np.mean(b * b))), 1e-30)
+
+
 def where_worst(got, want, meta=None):
     """Short description of where |got - want| is largest (for failure messages)."""
     got = np.asarray(got, np.float64)
