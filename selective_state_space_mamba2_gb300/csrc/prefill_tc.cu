@@ -1,4 +1,4 @@
-// Fused SSD prefill on the sm_103a tensor cores (bf16 operands, fp32 state).
+// Fused SSD prefill on the sm_103a tensor cores (bf16 inputs, fp32 state).
 //
 // The chunked scan of "[vllm] vLLM Mamba2 SSD 커널 웜업" (section
 // "mamba_mixer2.py 변경 사항 (핵심)"), fused into one kernel: one CTA walks one
@@ -27,12 +27,16 @@
 // at the group's last row e: exp(c_t - c_e) exp(c_e - c_s), both factors <= 1,
 // so only the diagonal group needs one exponential per element.
 //
-// Warp roles (192 threads, two CTAs per SM):
-//   warps 0-3  compute: scan of delta, w x, the P pass (TMEM -> TMEM),
-//              epilogue (TMEM -> y), state update; thread t owns TMEM lane t
-//              (token row t for S/Y, dstate row t for dS and the state)
-//   warp 4     TMA producer (C, B, x tiles; 128-byte swizzle)
-//   warp 5     TMEM allocation and MMA issue
+// One CTA per SM (320 threads):
+//   warps 0-7  compute, two warpgroups; thread (g, r) owns TMEM lane r (token
+//              row r of S and Y, dstate row r of dS and the state) and half of
+//              the columns: warpgroup g takes headdim [32g, 32g+32) of y and
+//              of the state, S column groups {g, g+2}, and converts C (g=0) or
+//              B (g=1)
+//   warp 8     TMA producer, C/B/x tiles double-buffered (128-byte swizzle)
+//   warp 9     TMEM allocation (512 columns) and MMA issue; M3/M4 of a block
+//              go out as soon as their fp16 operands exist, M2 when P is
+//              ready, then M1 of the next block
 // Every mbarrier wait is bounded; on a timeout the CTA reports
 // SSD_DEVERR_TIMEOUT, drains its own in-flight copies and MMAs, frees its
 // TMEM and exits.
@@ -63,29 +67,32 @@ using namespace tc;
 constexpr int kL = 128;  // tokens per block
 constexpr int kP = 64;   // headdim
 constexpr int kN = 128;  // dstate
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kCompute = 256;
+constexpr int kThreads = kCompute + 64;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
 // TMEM columns
-constexpr uint32_t COL_S = 0;    // S (128 fp32 columns); P (64 packed bf16x2 columns) overwrites its first half
-constexpr uint32_t COL_P = 0;
-constexpr uint32_t COL_DS = 64;  // dS, after the P pass has read S
-constexpr uint32_t COL_Y1 = 128;
-constexpr uint32_t COL_Y2 = 192;
+constexpr uint32_t COL_S0 = 0;    // S of even blocks (128 fp32 columns)
+constexpr uint32_t COL_S1 = 128;  // S of odd blocks
+constexpr uint32_t COL_Y1 = 256;
+constexpr uint32_t COL_Y2 = 320;
+constexpr uint32_t COL_DS = 384;
+constexpr uint32_t COL_P = 448;   // P, 64 columns of packed fp16 pairs
 // shared memory (offsets from the 1024-aligned dynamic base)
-constexpr uint32_t OFF_C = 0;        // C tile: two [128 x 64] bf16 atoms
-constexpr uint32_t OFF_B = 32768;    // B tile
-constexpr uint32_t OFF_X = 65536;    // x tile [128 tokens x 64]
-constexpr uint32_t OFF_XW = 81920;   // w-scaled x; reused to stage y
-constexpr uint32_t OFF_H = 98304;    // bf16 state entering the block, row n = 64 headdim values
-constexpr uint32_t OFF_F = 114688;   // column factors [128] fp32
-constexpr uint32_t OFF_WT = OFF_F + 512;   // per-warp sums of delta*A [4]
-constexpr uint32_t OFF_TM = OFF_WT + 16;   // TMEM base address
-constexpr uint32_t OFF_BAR = OFF_WT + 32;  // mbarriers
-constexpr uint32_t kSmemBytes = OFF_BAR + 8 * 8;
-constexpr uint32_t kTxBytes = 32768 + 32768 + 16384;
+constexpr uint32_t STAGE = 81920;          // C 32 KB | B 32 KB | x 16 KB
+constexpr uint32_t OFF_STAGE = 0;          // two stages
+constexpr uint32_t OFF_XW = 2 * STAGE;     // w x (fp16); reused to stage y
+constexpr uint32_t OFF_H = OFF_XW + 16384; // fp16 state entering the block
+constexpr uint32_t OFF_F = OFF_H + 16384;  // column factors, one copy per warpgroup [2][128]
+constexpr uint32_t OFF_CD = OFF_F + 1024;  // c_t and delta_t of every row, per warpgroup [2][2][128]
+constexpr uint32_t OFF_WT = OFF_CD + 2048; // per-warp sums of delta*A, per warpgroup [2][4]
+constexpr uint32_t OFF_TM = OFF_WT + 32;   // TMEM base address
+constexpr uint32_t OFF_BAR = OFF_TM + 16;  // mbarriers
+constexpr uint32_t kSmemBytes = OFF_BAR + 16 * 8;
+constexpr uint32_t kTxBytes = STAGE;
 
-enum { BAR_FULL = 0, BAR_EMPTY, BAR_S, BAR_P, BAR_ACC, BAR_DSFREE };
+enum { BAR_FULL0 = 0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_S0, BAR_S1, BAR_OPS, BAR_PRDY, BAR_ACC, BAR_DRAIN, BAR_COUNT };
+constexpr uint32_t BAR_VOTE = 3;  // named barrier of the 256 compute threads
 
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool v) {
     uint32_t r;
@@ -96,6 +103,15 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool v) {
         : "r"((uint32_t)v), "r"(id), "r"(n)
         : "memory");
     return r != 0;
+}
+
+// One lane per warp polls the barrier; the warp learns the outcome by shuffle.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity);
+    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+    __syncwarp();
+    return ok;
 }
 
 // Walks the blocks of one sequence: chunks [first, last], each cut into
@@ -121,16 +137,16 @@ struct Cursor {
     }
 };
 
-// fp16 copy of the state row (dstate row n = thread) into the M3 operand tile
-__device__ __forceinline__ void store_state_row(uint8_t *sH, int n, const float (&st)[kP]) {
+// fp16 copy of half a state row (dstate row n, headdim [32g, 32g+32)) into the M3 tile
+__device__ __forceinline__ void store_state_half(uint8_t *sH, int n, int g, const float (&st)[32]) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
         uint4 v;
         v.x = pack_f16_sat(st[8 * c + 0], st[8 * c + 1]);
         v.y = pack_f16_sat(st[8 * c + 2], st[8 * c + 3]);
         v.z = pack_f16_sat(st[8 * c + 4], st[8 * c + 5]);
         v.w = pack_f16_sat(st[8 * c + 6], st[8 * c + 7]);
-        *reinterpret_cast<uint4 *>(sH + sw128_offset(n, c)) = v;
+        *reinterpret_cast<uint4 *>(sH + sw128_offset(n, 4 * g + c)) = v;
     }
 }
 
@@ -146,7 +162,16 @@ __device__ __forceinline__ void tile_row_to_f16(uint8_t *tile, int r) {
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__device__ __forceinline__ void issue_m1(uint32_t tm_s, uint32_t aC, uint32_t aB) {
+    constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // raw bf16 C and B
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+        mma_ss(tm_s, sw128_desc(aC + ko, 16, 1024), sw128_desc(aB + ko, 16, 1024), kIdS, k > 0);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
     ssd_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -155,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int h = blockIdx.x - slot_r * p.H;
     const int r = p.seq_order ? p.seq_order[slot_r] : slot_r;
     if (r < 0 || r >= p.S) {
-        if (threadIdx.x == 0 && h == 0) report(p.err, SSD_DEVERR_METADATA);
+        if (tid == 0 && h == 0) report(p.err, SSD_DEVERR_METADATA);
         return;
     }
     const int g = h / (p.H / p.G);
@@ -182,19 +207,26 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (tid == 0) report(p.err, SSD_DEVERR_INTERNAL);
         return;
     }
-    uint8_t *sC = smem + OFF_C, *sB = smem + OFF_B, *sX = smem + OFF_X, *sXW = smem + OFF_XW, *sH = smem + OFF_H;
+    uint8_t *sXW = smem + OFF_XW, *sH = smem + OFF_H;
     float *sF = reinterpret_cast<float *>(smem + OFF_F);
     float *sWT = reinterpret_cast<float *>(smem + OFF_WT);
     uint32_t *sTM = reinterpret_cast<uint32_t *>(smem + OFF_TM);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    auto stage_c = [&](int s) { return smem + OFF_STAGE + s * STAGE; };
+    auto stage_b = [&](int s) { return smem + OFF_STAGE + s * STAGE + 32768; };
+    auto stage_x = [&](int s) { return smem + OFF_STAGE + s * STAGE + 65536; };
 
     if (tid == 0) {
-        mbar_init(&bar[BAR_FULL], 1);
-        mbar_init(&bar[BAR_EMPTY], 1);
-        mbar_init(&bar[BAR_S], 1);
-        mbar_init(&bar[BAR_P], 4);
+        mbar_init(&bar[BAR_FULL0], 1);
+        mbar_init(&bar[BAR_FULL1], 1);
+        mbar_init(&bar[BAR_EMPTY0], 1);
+        mbar_init(&bar[BAR_EMPTY1], 1);
+        mbar_init(&bar[BAR_S0], 1);
+        mbar_init(&bar[BAR_S1], 1);
+        mbar_init(&bar[BAR_OPS], 8);
+        mbar_init(&bar[BAR_PRDY], 8);
         mbar_init(&bar[BAR_ACC], 1);
-        mbar_init(&bar[BAR_DSFREE], 4);
+        mbar_init(&bar[BAR_DRAIN], 1);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -217,51 +249,42 @@ __global__ void __launch_bounds__(kThreads, 2)
             cur.start(p.cu_chunk, first, last);
             int issued = 0;
             for (int i = 0; i < nblocks; ++i, cur.next()) {
-                if (i > 0 && !mbar_wait(&bar[BAR_EMPTY], (i - 1) & 1)) {
+                const int s = i & 1, u = i >> 1;
+                if (u > 0 && !mbar_wait(&bar[BAR_EMPTY0 + s], (u - 1) & 1)) {
                     report(p.err, SSD_DEVERR_TIMEOUT);
                     break;
                 }
-                mbar_arrive_expect_tx(&bar[BAR_FULL], kTxBytes);
-                tma_load_3d(sC, &tmC, 0, g, cur.tb, &bar[BAR_FULL]);
-                tma_load_3d(sC + 16384, &tmC, 64, g, cur.tb, &bar[BAR_FULL]);
-                tma_load_3d(sB, &tmB, 0, g, cur.tb, &bar[BAR_FULL]);
-                tma_load_3d(sB + 16384, &tmB, 64, g, cur.tb, &bar[BAR_FULL]);
-                tma_load_3d(sX, &tmX, 0, h, cur.tb, &bar[BAR_FULL]);
+                uint64_t *full = &bar[BAR_FULL0 + s];
+                mbar_arrive_expect_tx(full, kTxBytes);
+                tma_load_3d(stage_c(s), &tmC, 0, g, cur.tb, full);
+                tma_load_3d(stage_c(s) + 16384, &tmC, 64, g, cur.tb, full);
+                tma_load_3d(stage_b(s), &tmB, 0, g, cur.tb, full);
+                tma_load_3d(stage_b(s) + 16384, &tmB, 64, g, cur.tb, full);
+                tma_load_3d(stage_x(s), &tmX, 0, h, cur.tb, full);
                 issued = i + 1;
             }
-            // drain: the last issued copy must land before the CTA may exit
-            if (issued > 0) mbar_wait(&bar[BAR_FULL], (issued - 1) & 1);
+            // drain: the copies in flight must land before the CTA may exit
+            for (int i = (issued >= 2 ? issued - 2 : 0); i < issued; ++i)
+                mbar_wait(&bar[BAR_FULL0 + (i & 1)], (i >> 1) & 1);
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            const uint32_t aC = smem_u32(sC), aB = smem_u32(sB), aX = smem_u32(sX), aXW = smem_u32(sXW),
-                           aH = smem_u32(sH);
-            constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // raw bf16 C and B
-            constexpr uint32_t kIdY = idesc_f16(128, 64, 0, 1);    // fp16 operands from here on
+            constexpr uint32_t kIdY = idesc_f16(128, 64, 0, 1);  // fp16 operands
             constexpr uint32_t kIdD = idesc_f16(128, 64, 1, 1);
-            int committed = 0;  // blocks whose final commit was issued
-            for (int i = 0; i < nblocks; ++i) {
-                const uint32_t ph = i & 1;
-                if (!mbar_wait(&bar[BAR_FULL], ph) || (i > 0 && !mbar_wait(&bar[BAR_DSFREE], (i - 1) & 1))) {
-                    report(p.err, SSD_DEVERR_TIMEOUT);
-                    break;
-                }
+            const uint32_t aXW = smem_u32(sXW), aH = smem_u32(sH);
+            bool ok = mbar_wait(&bar[BAR_FULL0], 0);
+            int m1_issued = 0;  // blocks whose M1 went out
+            if (ok) {
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_ss(tm + COL_S, sw128_desc(aC + ko, 16, 1024), sw128_desc(aB + ko, 16, 1024), kIdS, k > 0);
-                }
-                mma_commit(&bar[BAR_S]);
-                if (!mbar_wait(&bar[BAR_P], ph)) {
-                    report(p.err, SSD_DEVERR_TIMEOUT);
-                    mbar_wait(&bar[BAR_S], ph);  // drain M1
-                    break;
-                }
+                issue_m1(tm + COL_S0, smem_u32(stage_c(0)), smem_u32(stage_b(0)));
+                mma_commit(&bar[BAR_S0]);
+                m1_issued = 1;
+            }
+            for (int i = 0; ok && i < nblocks; ++i) {
+                const int s = i & 1;
+                const uint32_t aC = smem_u32(stage_c(s)), aB = smem_u32(stage_b(s)), aX = smem_u32(stage_x(s));
+                if (!(ok = mbar_wait(&bar[BAR_OPS], i & 1))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_ts(tm + COL_Y1, tm + COL_P + 8 * k, sw128_desc(aX + 2048 * k, 1024, 1024), kIdY, k > 0);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
@@ -270,45 +293,80 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_ss(tm + COL_DS, sw128_desc(aB + 2048 * k, 16384, 1024),
-                           sw128_desc(aXW + 2048 * k, 1024, 1024), kIdD, k > 0);
+                    mma_ss(tm + COL_DS, sw128_desc(aB + 2048 * k, 16384, 1024), sw128_desc(aXW + 2048 * k, 1024, 1024),
+                           kIdD, k > 0);
+                // M2 when P is ready; M1 of the next block after it (its S is needed only
+                // once this block's epilogue is done, and M2 is on the critical path)
+                ok = mbar_wait(&bar[BAR_PRDY], i & 1);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_ts(tm + COL_Y1, tm + COL_P + 8 * k, sw128_desc(aX + 2048 * k, 1024, 1024), kIdY, k > 0);
                 mma_commit(&bar[BAR_ACC]);
-                mma_commit(&bar[BAR_EMPTY]);
-                committed = i + 1;
+                mma_commit(&bar[BAR_EMPTY0 + s]);
+                if (m1_issued == i + 1 && i + 1 < nblocks) {
+                    const int s1 = (i + 1) & 1;
+                    if (!(ok = mbar_wait(&bar[BAR_FULL0 + s1], ((i + 1) >> 1) & 1))) break;
+                    tc_fence_after();
+                    issue_m1(tm + (s1 ? COL_S1 : COL_S0), smem_u32(stage_c(s1)), smem_u32(stage_b(s1)));
+                    mma_commit(&bar[BAR_S0 + s1]);
+                    ++m1_issued;
+                }
             }
-            if (committed > 0) mbar_wait(&bar[BAR_EMPTY], (committed - 1) & 1);  // drain
+            if (!ok) report(p.err, SSD_DEVERR_TIMEOUT);
+            // drain: one more commit covers every MMA this thread issued
+            mma_commit(&bar[BAR_DRAIN]);
+            mbar_wait(&bar[BAR_DRAIN], 0);
         }
     } else {
         // ------------------------------------------------ compute warps ----
-        const int t = tid;  // TMEM lane / token row / dstate row
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int wg = warp >> 2;            // warpgroup: headdim half and column groups
+        const int q = warp & 3;              // warp within the warpgroup
+        const int t = q * 32 + lane;         // TMEM lane / token row / dstate row
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const float Ah = p.A[h];
         const float Dh = p.D ? p.D[h] : 0.f;
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
         const size_t HPN = (size_t)p.H * kP * kN;
-        float st[kP];
+        float *myF = sF + wg * 128;
+        float *myWT = sWT + wg * 4;
+        float *myC = reinterpret_cast<float *>(smem + OFF_CD) + wg * 256;  // [128] c, then [128] delta
+        float *myD = myC + 128;
+        float st[32];  // state h[p][n = t] for p in [32 wg, 32 wg + 32)
         {
             const int32_t is = p.init_slot ? p.init_slot[r] : p.null_id;
-            if (slot_usable(is, p.null_id, p.num_slots, t == 0 ? p.err : nullptr)) {
-                const float *src = p.cache + (size_t)is * HPN + (size_t)h * kP * kN + t;
+            if (slot_usable(is, p.null_id, p.num_slots, (tid == 0) ? p.err : nullptr)) {
+                const float *src = p.cache + (size_t)is * HPN + (size_t)h * kP * kN + (size_t)(32 * wg) * kN + t;
 #pragma unroll
-                for (int q = 0; q < kP; ++q) st[q] = src[(size_t)q * kN];
+                for (int e = 0; e < 32; ++e) st[e] = src[(size_t)e * kN];
             } else {
 #pragma unroll
-                for (int q = 0; q < kP; ++q) st[q] = 0.f;
+                for (int e = 0; e < 32; ++e) st[e] = 0.f;
             }
         }
-        store_state_row(sH, t, st);
+        store_state_half(sH, t, wg, st);
 
         Cursor cur;
         cur.start(p.cu_chunk, first, last);
+        // dt of the next block is loaded one block ahead (its latency hides under this block)
+        __nv_bfloat16 dt_next = t < cur.len() ? p.dt[(size_t)(cur.tb + t) * p.H + h] : __float2bfloat16(0.f);
         for (int i = 0; i < nblocks; ++i, cur.next()) {
-            const uint32_t ph = i & 1;
+            const int s = i & 1;
+            const uint32_t ph = (i >> 1) & 1;
             const int tb = cur.tb, L = cur.len();
-            // ---- delta, in-block cumsum c_t, factors
+            uint8_t *sCs = stage_c(s), *sBs = stage_b(s), *sXs = stage_x(s);
+            const uint32_t colS = s ? COL_S1 : COL_S0;
+            const __nv_bfloat16 dt_cur = dt_next;
+            {
+                Cursor nx = cur;
+                nx.next();
+                if (i + 1 < nblocks && t < nx.len()) dt_next = p.dt[(size_t)(nx.tb + t) * p.H + h];
+            }
+            // ---- delta, in-block cumsum c_t, factors (each warpgroup on its own)
             float delta = 0.f, a = 0.f;
             if (t < L) {
-                const float v = __bfloat162float(p.dt[(size_t)(tb + t) * p.H + h]) + bias;
+                const float v = __bfloat162float(dt_cur) + bias;
                 delta = step_delta(v, p.dt_softplus, p.dt_min, p.dt_max);
                 a = delta * Ah;
             }
@@ -318,154 +376,153 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float v = __shfl_up_sync(0xffffffffu, c, off);
                 if (lane >= off) c += v;
             }
-            if (lane == 31) sWT[warp] = c;
-            named_bar_sync(1, 128);
+            if (lane == 31) myWT[q] = c;
+            named_bar_sync(1 + wg, 128);
             float wt[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) wt[j] = sWT[j];
+            for (int j = 0; j < 4; ++j) wt[j] = myWT[j];
             float prefix = 0.f, own = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (j < warp) prefix += wt[j];
-                if (j == warp) own = wt[j];
+                if (j < q) prefix += wt[j];
+                if (j == q) own = wt[j];
             }
-            c += prefix;                                     // c_t
+            c += prefix;                                  // c_t
             const float c_last = wt[0] + wt[1] + wt[2] + wt[3];
-            const float c_gend = prefix + own;              // c at the end of my group
-            sF[t] = __expf(c_gend - c) * delta;              // column factor of column t
-            const float w_x = __expf(c_last - c) * delta;    // state-update weight of token t
-            const float e_row = __expf(c);                   // carried-state factor of row t
+            myF[t] = __expf(prefix + own - c) * delta;     // column factor of column t
+            myC[t] = c;
+            myD[t] = delta;
+            const float w_x = __expf(c_last - c) * delta;  // state-update weight of token t
+            const float e_row = __expf(c);                 // carried-state factor of row t
             const float decay = __expf(c_last);
 
-            // ---- x tile landed: w x into the M4 operand tile
-            bool ok = mbar_wait(&bar[BAR_FULL], ph);
-            if (!named_bar_and(1, 128, ok)) {
-                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+            // ---- tiles landed: w x and x -> fp16 (this warpgroup's half of row t)
+            bool ok = warp_wait(&bar[BAR_FULL0 + s], ph);
+            if (!named_bar_and(BAR_VOTE, kCompute, ok)) {
+                if (tid == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
             }
-            {
-                // x row t: w x into the M4 operand (fp16) and x itself -> fp16 in place (M2 operand)
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint4 v = *reinterpret_cast<const uint4 *>(sX + sw128_offset(t, cc));
-                    uint4 xw;
-                    xw.x = pack_f16_sat(w_x * __uint_as_float(v.x << 16), w_x * __uint_as_float(v.x & 0xFFFF0000u));
-                    xw.y = pack_f16_sat(w_x * __uint_as_float(v.y << 16), w_x * __uint_as_float(v.y & 0xFFFF0000u));
-                    xw.z = pack_f16_sat(w_x * __uint_as_float(v.z << 16), w_x * __uint_as_float(v.z & 0xFFFF0000u));
-                    xw.w = pack_f16_sat(w_x * __uint_as_float(v.w << 16), w_x * __uint_as_float(v.w & 0xFFFF0000u));
-                    *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
-                    *reinterpret_cast<uint4 *>(sX + sw128_offset(t, cc)) = bf16x8_to_f16x8(v);
-                }
+            for (int cc = 4 * wg; cc < 4 * wg + 4; ++cc) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(sXs + sw128_offset(t, cc));
+                uint4 xw;
+                xw.x = pack_f16_sat(w_x * __uint_as_float(v.x << 16), w_x * __uint_as_float(v.x & 0xFFFF0000u));
+                xw.y = pack_f16_sat(w_x * __uint_as_float(v.y << 16), w_x * __uint_as_float(v.y & 0xFFFF0000u));
+                xw.z = pack_f16_sat(w_x * __uint_as_float(v.z << 16), w_x * __uint_as_float(v.z & 0xFFFF0000u));
+                xw.w = pack_f16_sat(w_x * __uint_as_float(v.w << 16), w_x * __uint_as_float(v.w & 0xFFFF0000u));
+                *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
+                *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = bf16x8_to_f16x8(v);
             }
-            // ---- S ready: P pass, S (fp32) -> P (bf16) in TMEM
-            ok = mbar_wait(&bar[BAR_S], ph);
-            if (!named_bar_and(1, 128, ok)) {  // also publishes sF to the compute warps
-                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+            // ---- S ready (M1 is done with the raw tiles): C or B row t -> fp16
+            ok = warp_wait(&bar[BAR_S0 + s], ph);
+            if (!named_bar_and(BAR_VOTE, kCompute, ok)) {
+                if (tid == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
+            tile_row_to_f16(wg == 0 ? sCs : sBs, t);
+            fence_proxy_async_smem();  // w x, x, B, C and the state tile -> async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[BAR_OPS]);
+
+            // ---- P pass: S (fp32) -> P (fp16) in TMEM, column groups {wg, wg + 2}
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = wg + 2 * jj;
                 uint32_t pk[16];
-                if (j < warp) {
+                if (j < q) {
                     uint32_t v[32];
-                    tmem_ld32(tm + lane_base + COL_S + 32 * j, v);
+                    tmem_ld32(tm + lane_base + colS + 32 * j, v);
                     tmem_ld_wait();
                     float gend = 0.f;
 #pragma unroll
-                    for (int q = 0; q <= j; ++q) gend += wt[q];
+                    for (int u = 0; u < 4; ++u)
+                        if (u <= j) gend += wt[u];
                     const float R = __expf(c - gend);
-                    const float4 *f4 = reinterpret_cast<const float4 *>(sF + 32 * j);
+                    const float4 *f4 = reinterpret_cast<const float4 *>(myF + 32 * j);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 f = f4[q];
-                        pk[2 * q] = pack_f16_sat(__uint_as_float(v[4 * q]) * f.x * R, __uint_as_float(v[4 * q + 1]) * f.y * R);
-                        pk[2 * q + 1] = pack_f16_sat(__uint_as_float(v[4 * q + 2]) * f.z * R,
-                                                     __uint_as_float(v[4 * q + 3]) * f.w * R);
+                    for (int u = 0; u < 8; ++u) {
+                        const float4 f = f4[u];
+                        pk[2 * u] = pack_f16_sat(__uint_as_float(v[4 * u]) * f.x * R, __uint_as_float(v[4 * u + 1]) * f.y * R);
+                        pk[2 * u + 1] = pack_f16_sat(__uint_as_float(v[4 * u + 2]) * f.z * R,
+                                                     __uint_as_float(v[4 * u + 3]) * f.w * R);
                     }
-                } else if (j == warp) {
+                } else if (j == q) {
+                    // diagonal group: one exponential per element, branch-free (c, delta of the
+                    // columns by broadcast from shared memory; the mask by select)
                     uint32_t v[32];
-                    tmem_ld32(tm + lane_base + COL_S + 32 * j, v);
+                    tmem_ld32(tm + lane_base + colS + 32 * j, v);
                     tmem_ld_wait();
-                    float pv[32];
+                    const float4 *c4 = reinterpret_cast<const float4 *>(myC + 32 * j);
+                    const float4 *d4 = reinterpret_cast<const float4 *>(myD + 32 * j);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const float cs_s = __shfl_sync(0xffffffffu, c, q);
-                        const float d_s = __shfl_sync(0xffffffffu, delta, q);
-                        float val = q <= lane ? __uint_as_float(v[q]) * __expf(c - cs_s) * d_s : 0.f;
-                        if (q == lane) val += Dh;
-                        pv[q] = val;
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 cs = c4[u4], ds = d4[u4];
+                        const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, dv[4] = {ds.x, ds.y, ds.z, ds.w};
+                        float pv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int u = 4 * u4 + e;
+                            const float ex = __expf(fminf(c - cv[e], 0.f));
+                            const float val = __uint_as_float(v[u]) * ex * dv[e];
+                            pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
+                        }
+                        pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
+                        pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
                     }
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) pk[q] = pack_f16_sat(pv[2 * q], pv[2 * q + 1]);
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) pk[q] = 0u;
+                    for (int u = 0; u < 16; ++u) pk[u] = 0u;
                 }
                 tmem_st16(tm + lane_base + COL_P + 16 * j, pk);
             }
-            // M1 is done with the raw tiles: C and B rows -> fp16 for M3 and M4
-            tile_row_to_f16(sC, t);
-            tile_row_to_f16(sB, t);
             tmem_st_wait();
-            fence_proxy_async_smem();  // w x, x, B, C and the state tile -> async proxy
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[BAR_P]);
+            if (lane == 0) mbar_arrive(&bar[BAR_PRDY]);
 
             // ---- accumulators ready
-            ok = mbar_wait(&bar[BAR_ACC], ph);
-            if (!named_bar_and(1, 128, ok)) {
-                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+            ok = warp_wait(&bar[BAR_ACC], i & 1);
+            if (!named_bar_and(BAR_VOTE, kCompute, ok)) {
+                if (tid == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
             {
-                uint32_t d0[32], d1[32];
-                tmem_ld32(tm + lane_base + COL_DS, d0);
-                tmem_ld32(tm + lane_base + COL_DS + 32, d1);
+                uint32_t d[32], y1[32], y2[32];
+                tmem_ld32(tm + lane_base + COL_DS + 32 * wg, d);
+                tmem_ld32(tm + lane_base + COL_Y1 + 32 * wg, y1);
+                tmem_ld32(tm + lane_base + COL_Y2 + 32 * wg, y2);
                 tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[BAR_DSFREE]);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    st[q] = fmaf(decay, st[q], __uint_as_float(d0[q]));
-                    st[32 + q] = fmaf(decay, st[32 + q], __uint_as_float(d1[q]));
-                }
-            }
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t y1[32], y2[32];
-                tmem_ld32(tm + lane_base + COL_Y1 + 32 * half, y1);
-                tmem_ld32(tm + lane_base + COL_Y2 + 32 * half, y2);
-                tmem_ld_wait();
+                for (int e = 0; e < 32; ++e) st[e] = fmaf(decay, st[e], __uint_as_float(d[e]));
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint4 v;
                     uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int e = 8 * cc + 2 * q;
-                        vv[q] = pack_bf16(fmaf(e_row, __uint_as_float(y2[e]), __uint_as_float(y1[e])),
+                    for (int u = 0; u < 4; ++u) {
+                        const int e = 8 * cc + 2 * u;
+                        vv[u] = pack_bf16(fmaf(e_row, __uint_as_float(y2[e]), __uint_as_float(y1[e])),
                                           fmaf(e_row, __uint_as_float(y2[e + 1]), __uint_as_float(y1[e + 1])));
                     }
-                    *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, 4 * half + cc)) = v;
+                    *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, 4 * wg + cc)) = v;
                 }
             }
-            store_state_row(sH, t, st);
+            tc_fence_before();
+            store_state_half(sH, t, wg, st);
             if (cur.ends_chunk()) {
                 const int32_t cs = p.chunk_slot ? p.chunk_slot[cur.k] : p.null_id;
-                if (slot_usable(cs, p.null_id, p.num_slots, t == 0 ? p.err : nullptr)) {
-                    float *dst = p.cache + (size_t)cs * HPN + (size_t)h * kP * kN + t;
+                if (slot_usable(cs, p.null_id, p.num_slots, (tid == 0) ? p.err : nullptr)) {
+                    float *dst = p.cache + (size_t)cs * HPN + (size_t)h * kP * kN + (size_t)(32 * wg) * kN + t;
 #pragma unroll
-                    for (int q = 0; q < kP; ++q) dst[(size_t)q * kN] = st[q];
+                    for (int e = 0; e < 32; ++e) dst[(size_t)e * kN] = st[e];
                 }
             }
-            named_bar_sync(1, 128);  // y tile staged
+            named_bar_sync(BAR_VOTE, kCompute);  // y tile staged
 #pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                const int row = rr * 16 + (t >> 3), cc = t & 7;
+            for (int rr = 0; rr < 4; ++rr) {
+                const int row = rr * 32 + (tid >> 3), cc = tid & 7;
                 if (row < L) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(sXW + sw128_offset(row, cc));
                     *reinterpret_cast<uint4 *>(p.y + ((size_t)(tb + row) * p.H + h) * kP + 8 * cc) = v;
