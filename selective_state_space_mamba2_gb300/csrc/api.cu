@@ -55,14 +55,15 @@ extern "C" int32_t ssd_abi_version(void) { return SSD_ABI_VERSION; }
 
 extern "C" size_t ssd_prefill_workspace_size(const ssd_prefill_args *a) {
     if (check_prefill(a) != SSD_OK) return 0;
-    if (a->total_tokens == 0 || ssd::tc_prefill_supported(*a)) return 0;
+    if (a->total_tokens == 0) return 0;
+    if (ssd::tc_prefill_supported(*a)) return ssd::tc_prefill_workspace(*a);
     return ssd::simt_prefill_workspace(*a, nullptr, nullptr);
 }
 
 extern "C" int32_t ssd_prefill_kernel_count(const ssd_prefill_args *a) {
     if (check_prefill(a) != SSD_OK) return -1;
     if (a->total_tokens == 0) return 0;
-    return ssd::tc_prefill_supported(*a) ? 1 : 4;
+    return ssd::tc_prefill_supported(*a) ? 2 : 4;
 }
 
 extern "C" ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *a, void *workspace,
@@ -71,7 +72,12 @@ extern "C" ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *a, void *work
     if (st != SSD_OK || a->total_tokens == 0) return st;
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     // bf16 with headdim 64 and dstate 128: the fused tensor-core kernel
-    if (ssd::tc_prefill_supported(*a)) return from_cuda(ssd::tc_prefill_launch(*a, cs));
+    if (ssd::tc_prefill_supported(*a)) {
+        if (!workspace || workspace_bytes < ssd::tc_prefill_workspace(*a) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return SSD_ERR_WORKSPACE;
+        return from_cuda(ssd::tc_prefill_launch(*a, workspace, cs));
+    }
     if (!ssd::simt_prefill_supported(*a)) return SSD_ERR_UNSUPPORTED;
     const size_t need = ssd::simt_prefill_workspace(*a, nullptr, nullptr);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))

@@ -64,7 +64,8 @@ cudaError_t simt_prefill_launch(const ssd_prefill_args &a, const PrefillWorkspac
 bool simt_prefill_supported(const ssd_prefill_args &a);
 
 bool tc_prefill_supported(const ssd_prefill_args &a);
-cudaError_t tc_prefill_launch(const ssd_prefill_args &a, cudaStream_t s);
+size_t tc_prefill_workspace(const ssd_prefill_args &a);
+cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s);
 
 bool decode_supported(const ssm_decode_args &a);
 cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s);

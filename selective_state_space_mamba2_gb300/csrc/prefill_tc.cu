@@ -44,6 +44,8 @@
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
+#include <algorithm>
+
 namespace ssd {
 
 struct TcParams {
@@ -114,6 +116,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     return ok;
 }
 
+// delta = clamp(softplus(v), lo, hi) from the fast exp/log intrinsics:
+// softplus(v) = v above 15 (the rest is below e^-15 relative); e - e^2/2 with
+// e = exp(v) below -5 (log1p's series; the next term is under 2e-5
+// relative there); log(1 + e) in between, where 1 + e >= 1.0067 keeps the
+// rounding of the sum under 1e-5 relative.
+__device__ __forceinline__ float fast_delta(float v, int dt_softplus, float lo, float hi) {
+    float d = v;
+    if (dt_softplus && v <= 15.f) {
+        const float e = __expf(v);
+        d = v < -5.f ? e * (1.f - 0.5f * e) : __logf(1.f + e);
+    }
+    return fminf(fmaxf(d, lo), hi);
+}
+
 // Walks the blocks of one sequence: chunks [first, last], each cut into
 // blocks of at most kL tokens that never cross a chunk end.
 struct Cursor {
@@ -150,20 +166,8 @@ __device__ __forceinline__ void store_state_half(uint8_t *sH, int n, int g, cons
     }
 }
 
-// row r of a [128 x 128] bf16 tile held as two 64-wide swizzled atoms -> fp16, in place
-__device__ __forceinline__ void tile_row_to_f16(uint8_t *tile, int r) {
-#pragma unroll
-    for (int a = 0; a < 2; ++a) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 *q = reinterpret_cast<uint4 *>(tile + a * 16384 + sw128_offset(r, c));
-            *q = bf16x8_to_f16x8(*q);
-        }
-    }
-}
-
 __device__ __forceinline__ void issue_m1(uint32_t tm_s, uint32_t aC, uint32_t aB) {
-    constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 0);  // raw bf16 C and B
+    constexpr uint32_t kIdS = idesc_f16(128, 128, 0, 0);  // fp16 C and B (converted once per call)
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float delta = 0.f, a = 0.f;
             if (t < L) {
                 const float v = __bfloat162float(dt_cur) + bias;
-                delta = step_delta(v, p.dt_softplus, p.dt_min, p.dt_max);
+                delta = fast_delta(v, p.dt_softplus, p.dt_min, p.dt_max);
                 a = delta * Ah;
             }
             float c = a;
@@ -413,15 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
                 *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = bf16x8_to_f16x8(v);
             }
-            // ---- S ready (M1 is done with the raw tiles): C or B row t -> fp16
+            // ---- S ready
             ok = warp_wait(&bar[BAR_S0 + s], ph);
             if (!named_bar_and(BAR_VOTE, kCompute, ok)) {
                 if (tid == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            tile_row_to_f16(wg == 0 ? sCs : sBs, t);
-            fence_proxy_async_smem();  // w x, x, B, C and the state tile -> async proxy
+            fence_proxy_async_smem();  // w x, x and the state tile -> async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[BAR_OPS]);
 
@@ -538,18 +541,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// B and C (bf16) -> fp16 once per call: every head of a group reads the same
+// tiles, so converting them here instead of in each head's CTA saves the
+// per-CTA conversion work (and its shared-memory traffic) H/G times over.
+__global__ void __launch_bounds__(256) bc_to_f16_kernel(const uint4 *__restrict__ B, const uint4 *__restrict__ C,
+                                                        uint4 *__restrict__ Bh, uint4 *__restrict__ Ch, size_t n16) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
+        Bh[i] = bf16x8_to_f16x8(B[i]);
+        Ch[i] = bf16x8_to_f16x8(C[i]);
+    }
+}
+
 }  // namespace
+
+size_t tc_prefill_workspace(const ssd_prefill_args &a) {
+    const size_t bc = (size_t)a.total_tokens * a.ngroups * kN * 2;
+    return 2 * ((bc + 255) & ~(size_t)255);
+}
 
 bool tc_prefill_supported(const ssd_prefill_args &a) {
     return a.dtype == SSD_BF16 && a.headdim == kP && a.dstate == kN && a.total_tokens > 0;
 }
 
-cudaError_t tc_prefill_launch(const ssd_prefill_args &a, cudaStream_t s) {
+cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s) {
     CUtensorMap mX, mB, mC;
     const uint64_t T = (uint64_t)a.total_tokens;
+    const size_t bc = (size_t)a.total_tokens * a.ngroups * kN * 2;
+    uint8_t *Bh = static_cast<uint8_t *>(workspace);
+    uint8_t *Ch = Bh + ((bc + 255) & ~(size_t)255);
+    {
+        const size_t n16 = bc / 16;  // kN * 2 bytes per row: a multiple of 16
+        const int blocks = (int)std::min<size_t>((n16 + 255) / 256, 152 * 8);
+        bc_to_f16_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4 *>(a.B), static_cast<const uint4 *>(a.C),
+                                                reinterpret_cast<uint4 *>(Bh), reinterpret_cast<uint4 *>(Ch), n16);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (!make_tmap_bf16_3d(&mX, a.x, kP, a.nheads, T, (uint64_t)kP * 2, (uint64_t)a.nheads * kP * 2, 64, 1, kL) ||
-        !make_tmap_bf16_3d(&mB, a.B, kN, a.ngroups, T, (uint64_t)kN * 2, (uint64_t)a.ngroups * kN * 2, 64, 1, kL) ||
-        !make_tmap_bf16_3d(&mC, a.C, kN, a.ngroups, T, (uint64_t)kN * 2, (uint64_t)a.ngroups * kN * 2, 64, 1, kL))
+        !make_tmap_f16_3d(&mB, Bh, kN, a.ngroups, T, (uint64_t)kN * 2, (uint64_t)a.ngroups * kN * 2, 64, 1, kL) ||
+        !make_tmap_f16_3d(&mC, Ch, kN, a.ngroups, T, (uint64_t)kN * 2, (uint64_t)a.ngroups * kN * 2, 64, 1, kL))
         return cudaErrorInvalidValue;
     TcParams p;
     p.T = a.total_tokens;
