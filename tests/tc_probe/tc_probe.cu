@@ -10,6 +10,8 @@
 //   O3 = Cg Hg    (SS, K-major A, MN-major B)
 //   O4 = Bg^T Wg  (SS, MN-major A over two 64-wide atoms, MN-major B)
 //   O5 = Bg^T Wg  with the two descriptor offsets of A swapped (diagnostic)
+//   O6 = Cg [Hg | Wg]  (SS, K-major A, MN-major B over two 64-wide atoms, N=128;
+//                       a second phase, after O1..O5 were read)
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -27,7 +29,7 @@ __global__ void __launch_bounds__(128, 1) probe_kernel(const __grid_constant__ C
                                                         const __grid_constant__ CUtensorMap tmX,
                                                         const __nv_bfloat16 *Hg, const __nv_bfloat16 *Wg,
                                                         const __nv_bfloat16 *Pg, float *O1, float *O2, float *O3,
-                                                        float *O4, float *O5, int *status) {
+                                                        float *O4, float *O5, float *O6, int *status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sC = smem;              // 32 KB: two [128 x 64] atoms
@@ -42,6 +44,7 @@ __global__ void __launch_bounds__(128, 1) probe_kernel(const __grid_constant__ C
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(128, 1) probe_kernel(const __grid_constant__ C
         }
     }
     __syncthreads();
-    const bool ok = mbar_wait(&bars[1], 0);
+    const bool ok = mbar_wait(&bars[1], 0);  // also gates phase 2
     if (!ok) atomicOr(status, 2);
     tc_fence_after();
     if (ok) {
@@ -132,6 +135,34 @@ __global__ void __launch_bounds__(128, 1) probe_kernel(const __grid_constant__ C
                 for (int i = 0; i < 32; ++i) outs[o][row * 64 + 32 * j + i] = __uint_as_float(r[i]);
             }
     }
+    // phase 2: the H and W tiles are adjacent 16 KB atoms, one MN-major B operand with N = 128
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t aC = smem_u32(sC), aH = smem_u32(sH);
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
+            mma_ss(tm + 0, sw128_desc(aC + koff, 16, 1024), sw128_desc(aH + 2048 * k, 16384, 1024),
+                   idesc_bf16(128, 128, 0, 1), k > 0);
+        }
+        mma_commit(&bars[2]);
+    }
+    __syncthreads();
+    if (ok) {
+        const bool ok2 = mbar_wait(&bars[2], 0);
+        if (!ok2) atomicOr(status, 4);
+        tc_fence_after();
+        if (ok2) {
+            const int row = warp * 32 + lane;
+            uint32_t r[32];
+            for (int j = 0; j < 4; ++j) {
+                tmem_ld32(tmem_addr(tm, warp * 32, 32 * j), r);
+                tmem_ld_wait();
+                for (int i = 0; i < 32; ++i) O6[row * 128 + 32 * j + i] = __uint_as_float(r[i]);
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -143,8 +174,8 @@ __global__ void __launch_bounds__(128, 1) probe_kernel(const __grid_constant__ C
 }  // namespace
 
 extern "C" int tc_probe_run(const void *Cg, const void *Bg, const void *Xg, const void *Hg, const void *Wg,
-                            const void *Pg, float *O1, float *O2, float *O3, float *O4, float *O5, int *status,
-                            void *stream) {
+                            const void *Pg, float *O1, float *O2, float *O3, float *O4, float *O5, float *O6,
+                            int *status, void *stream) {
     CUtensorMap mC, mB, mX;
     if (!ssd::make_tmap_bf16_3d(&mC, Cg, 128, 1, 128, 256, 256, 64, 1, 128)) return 1;
     if (!ssd::make_tmap_bf16_3d(&mB, Bg, 128, 1, 128, 256, 256, 64, 1, 128)) return 2;
@@ -153,6 +184,6 @@ extern "C" int tc_probe_run(const void *Cg, const void *Bg, const void *Xg, cons
         return 4;
     probe_kernel<<<1, 128, kSmem + 1024, static_cast<cudaStream_t>(stream)>>>(
         mC, mB, mX, static_cast<const __nv_bfloat16 *>(Hg), static_cast<const __nv_bfloat16 *>(Wg),
-        static_cast<const __nv_bfloat16 *>(Pg), O1, O2, O3, O4, O5, status);
+        static_cast<const __nv_bfloat16 *>(Pg), O1, O2, O3, O4, O5, O6, status);
     return cudaGetLastError() == cudaSuccess ? 0 : 5;
 }

@@ -30,7 +30,8 @@ def test_tensor_core_forms_match_matmul():
     r = lambda *s: torch.randn(*s, generator=g, device="cuda").to(torch.bfloat16)
     C, B, X, H, W, P = r(128, 128), r(128, 128), r(128, 64), r(128, 64), r(128, 64), r(128, 128)
     outs = [torch.full((128, 128), float("nan"), device="cuda")] + \
-        [torch.full((128, 64), float("nan"), device="cuda") for _ in range(4)]
+        [torch.full((128, 64), float("nan"), device="cuda") for _ in range(4)] + \
+        [torch.full((128, 128), float("nan"), device="cuda")]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     p = lambda t: ctypes.c_void_p(t.data_ptr())
     rc = lib.tc_probe_run(p(C), p(B), p(X), p(H), p(W), p(P), *[p(o) for o in outs], p(status),
@@ -38,9 +39,11 @@ def test_tensor_core_forms_match_matmul():
     torch.cuda.synchronize()
     assert rc == 0 and int(status.item()) == 0
     d = lambda t: t.double()
-    want = [d(C) @ d(B).T, d(P) @ d(X), d(C) @ d(H), d(B).T @ d(W)]
-    names = ["C.B^T (SS, K/K)", "P.X (TS, MN B)", "C.H (SS, K A, MN B)", "B^T.W (SS, MN A, MN B)"]
-    errs = [float((d(o) - w).abs().max() / w.abs().max()) for o, w in zip(outs[:4], want)]
+    want = [d(C) @ d(B).T, d(P) @ d(X), d(C) @ d(H), d(B).T @ d(W), None, d(C) @ torch.cat([d(H), d(W)], 1)]
+    names = ["C.B^T (SS, K/K)", "P.X (TS, MN B)", "C.H (SS, K A, MN B)", "B^T.W (SS, MN A, MN B)", None,
+             "C.[H|W] (SS, K A, MN B, N=128)"]
+    errs = [float((d(o) - w).abs().max() / w.abs().max()) for o, w in zip(outs, want) if w is not None]
+    names = [n for n in names if n is not None]
     swapped = float((d(outs[4]) - want[3]).abs().max() / want[3].abs().max())
     msg = "; ".join("%s %.2e" % (n, e) for n, e in zip(names, errs)) + "; B^T.W swapped offsets %.2e" % swapped
     print(msg)
