@@ -9,12 +9,10 @@
 // 프리픽스 캐싱" on "[vLLM] Mamba (SSM): 선형 시간 복잡도 시퀀스 모델링").
 //
 // Per block of L <= 128 tokens [tb, tb+L) with in-block cumsum c_t of
-// delta*A, the four dense contractions run as tcgen05.mma tiles (fp32
-// accumulators).  M1 takes the bf16 inputs as they are; the operands the
-// kernel forms itself (P, w x, the carried state) are rounded to fp16, whose
-// 11-bit significand keeps their rounding error 8x below bf16's, and the x, B
-// and C tiles they meet are converted to fp16 in shared memory (exactly, for
-// values in fp16's range) because both operands of an MMA share one type:
+// delta*A, the four dense contractions run as tcgen05.mma tiles with fp32
+// accumulators and fp16 operands (B and C are converted once per call by a
+// small kernel; x, P, w x and the carried state are rounded to fp16, whose
+// 11-bit significand keeps their rounding error 8x below bf16's):
 //   M1  S  = C B^T                  [128 x 128], K = dstate   (SS, K/K-major)
 //   M2  Y1 = P X                    [128 x  64], K = tokens   (TS: P in TMEM)
 //        P[t,s] = exp(c_t - c_s) delta_s S[t,s] for s <= t, plus D on the diagonal
@@ -27,19 +25,19 @@
 // at the group's last row e: exp(c_t - c_e) exp(c_e - c_s), both factors <= 1,
 // so only the diagonal group needs one exponential per element.
 //
-// One CTA per SM (320 threads):
-//   warps 0-7  compute, two warpgroups; thread (g, r) owns TMEM lane r (token
-//              row r of S and Y, dstate row r of dS and the state) and half of
-//              the columns: warpgroup g takes headdim [32g, 32g+32) of y and
-//              of the state, S column groups {g, g+2}, and converts C (g=0) or
-//              B (g=1)
+// Only the state itself is a serial dependency from block to block (64 FMAs
+// per thread); everything else is pipelined.  One CTA per SM, 320 threads:
+//   warps 0-3  "producer" warpgroup, one block ahead: delta and the cumsum,
+//              w x and x -> fp16, the P pass (S -> P in TMEM, in place)
+//   warps 4-7  "consumer" warpgroup: state update, the fp16 state tile for
+//              the next block's M3, the chunk-boundary stores, y and its
+//              coalesced copy-out
 //   warp 8     TMA producer, C/B/x tiles double-buffered (128-byte swizzle)
-//   warp 9     TMEM allocation (512 columns) and MMA issue; M3/M4 of a block
-//              go out as soon as their fp16 operands exist, M2 when P is
-//              ready, then M1 of the next block
-// Every mbarrier wait is bounded; on a timeout the CTA reports
-// SSD_DEVERR_TIMEOUT, drains its own in-flight copies and MMAs, frees its
-// TMEM and exits.
+//   warp 9     TMEM allocation (512 columns) and MMA issue
+// Thread t of a warpgroup owns TMEM lane t: token row t of S, Y1, Y2 and
+// dstate row t of dS and of the state.  Every mbarrier wait is bounded; on a
+// timeout the CTA reports SSD_DEVERR_TIMEOUT, drains its own in-flight copies
+// and MMAs, frees its TMEM and exits.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -69,32 +67,45 @@ using namespace tc;
 constexpr int kL = 128;  // tokens per block
 constexpr int kP = 64;   // headdim
 constexpr int kN = 128;  // dstate
-constexpr int kCompute = 256;
-constexpr int kThreads = kCompute + 64;
+constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns
-constexpr uint32_t COL_S0 = 0;    // S of even blocks (128 fp32 columns)
-constexpr uint32_t COL_S1 = 128;  // S of odd blocks
-constexpr uint32_t COL_Y1 = 256;
-constexpr uint32_t COL_Y2 = 320;
-constexpr uint32_t COL_DS = 384;
-constexpr uint32_t COL_P = 448;   // P, 64 columns of packed fp16 pairs
+constexpr uint32_t COL_S0 = 0;     // S of even blocks (128 fp32 columns); P over its first 64
+constexpr uint32_t COL_S1 = 128;   // S of odd blocks
+constexpr uint32_t COL_Y1 = 256;   // P X
+constexpr uint32_t COL_Y2 = 320;   // C Hprev^T, even / odd blocks at +0 / +64
+constexpr uint32_t COL_DS = 448;   // B^T (w x)
 // shared memory (offsets from the 1024-aligned dynamic base)
-constexpr uint32_t STAGE = 81920;          // C 32 KB | B 32 KB | x 16 KB
-constexpr uint32_t OFF_STAGE = 0;          // two stages
-constexpr uint32_t OFF_XW = 2 * STAGE;     // w x (fp16); reused to stage y
-constexpr uint32_t OFF_H = OFF_XW + 16384; // fp16 state entering the block
-constexpr uint32_t OFF_F = OFF_H + 16384;  // column factors, one copy per warpgroup [2][128]
-constexpr uint32_t OFF_CD = OFF_F + 1024;  // c_t and delta_t of every row, per warpgroup [2][2][128]
-constexpr uint32_t OFF_WT = OFF_CD + 2048; // per-warp sums of delta*A, per warpgroup [2][4]
-constexpr uint32_t OFF_TM = OFF_WT + 32;   // TMEM base address
-constexpr uint32_t OFF_BAR = OFF_TM + 16;  // mbarriers
+constexpr uint32_t STAGE = 81920;            // C 32 KB | B 32 KB | x 16 KB
+constexpr uint32_t OFF_XW = 2 * STAGE;       // w x (fp16)
+constexpr uint32_t OFF_H = OFF_XW + 16384;   // fp16 state entering the block
+constexpr uint32_t OFF_Y = OFF_H + 16384;    // y staging (bf16)
+constexpr uint32_t OFF_F = OFF_Y + 16384;    // column factors [128]
+constexpr uint32_t OFF_CD = OFF_F + 512;     // c_t and delta_t [2][128]
+constexpr uint32_t OFF_E = OFF_CD + 1024;    // exp(c_t) per block, ring of 4 [4][128]
+constexpr uint32_t OFF_DEC = OFF_E + 2048;   // exp(c_L) per block, ring of 4
+constexpr uint32_t OFF_WT = OFF_DEC + 16;    // warp sums of delta*A [4]
+constexpr uint32_t OFF_TM = OFF_WT + 16;     // TMEM base address
+constexpr uint32_t OFF_BAR = OFF_TM + 16;    // mbarriers
 constexpr uint32_t kSmemBytes = OFF_BAR + 16 * 8;
-constexpr uint32_t kTxBytes = STAGE;
+constexpr int kRing = 4;
 
-enum { BAR_FULL0 = 0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_S0, BAR_S1, BAR_OPS, BAR_PRDY, BAR_ACC, BAR_DRAIN, BAR_COUNT };
-constexpr uint32_t BAR_VOTE = 3;  // named barrier of the 256 compute threads
+enum {
+    FULL0 = 0, FULL1, EMPTY0, EMPTY1, S_RDY0, S_RDY1,  // tiles and S, per stage
+    OPS_W,     // producer wg: w x and fp16 x of the block are in smem          (4 arrivals)
+    PRDY,      // producer wg: P of the block is in TMEM                        (4)
+    OPS_H,     // consumer wg: fp16 state entering the block is in smem         (4)
+    DS_FREE,   // consumer wg: read dS of the previous block                    (4)
+    Y1_FREE,   // consumer wg: read Y1 of the previous block                    (4)
+    ACC_DS,    // M4 of the block done (also frees w x)
+    H_FREE,    // M3 of the block done (the state tile may be rewritten)
+    ACC_Y,     // M2 and M3 of the block done
+    DRAIN,
+    NBAR
+};
+constexpr uint32_t BAR_PG = 1;  // named barrier of the producer warpgroup
+constexpr uint32_t BAR_CG = 2;  // named barrier of the consumer warpgroup
 
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool v) {
     uint32_t r;
@@ -153,25 +164,16 @@ struct Cursor {
     }
 };
 
-// fp16 copy of half a state row (dstate row n, headdim [32g, 32g+32)) into the M3 tile
-__device__ __forceinline__ void store_state_half(uint8_t *sH, int n, int g, const float (&st)[32]) {
+// fp16 copy of a state row (dstate row n: its 64 headdim values) into the M3 operand tile
+__device__ __forceinline__ void store_state_row(uint8_t *sH, int n, const float (&st)[kP]) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 8; ++c) {
         uint4 v;
         v.x = pack_f16_sat(st[8 * c + 0], st[8 * c + 1]);
         v.y = pack_f16_sat(st[8 * c + 2], st[8 * c + 3]);
         v.z = pack_f16_sat(st[8 * c + 4], st[8 * c + 5]);
         v.w = pack_f16_sat(st[8 * c + 6], st[8 * c + 7]);
-        *reinterpret_cast<uint4 *>(sH + sw128_offset(n, 4 * g + c)) = v;
-    }
-}
-
-__device__ __forceinline__ void issue_m1(uint32_t tm_s, uint32_t aC, uint32_t aB) {
-    constexpr uint32_t kIdS = idesc_f16(128, 128, 0, 0);  // fp16 C and B (converted once per call)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-        mma_ss(tm_s, sw128_desc(aC + ko, 16, 1024), sw128_desc(aB + ko, 16, 1024), kIdS, k > 0);
+        *reinterpret_cast<uint4 *>(sH + sw128_offset(n, c)) = v;
     }
 }
 
@@ -211,26 +213,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) report(p.err, SSD_DEVERR_INTERNAL);
         return;
     }
-    uint8_t *sXW = smem + OFF_XW, *sH = smem + OFF_H;
+    uint8_t *sXW = smem + OFF_XW, *sH = smem + OFF_H, *sY = smem + OFF_Y;
     float *sF = reinterpret_cast<float *>(smem + OFF_F);
+    float *sCc = reinterpret_cast<float *>(smem + OFF_CD);
+    float *sDl = sCc + 128;
+    float *sE = reinterpret_cast<float *>(smem + OFF_E);
+    float *sDec = reinterpret_cast<float *>(smem + OFF_DEC);
     float *sWT = reinterpret_cast<float *>(smem + OFF_WT);
     uint32_t *sTM = reinterpret_cast<uint32_t *>(smem + OFF_TM);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    auto stage_c = [&](int s) { return smem + OFF_STAGE + s * STAGE; };
-    auto stage_b = [&](int s) { return smem + OFF_STAGE + s * STAGE + 32768; };
-    auto stage_x = [&](int s) { return smem + OFF_STAGE + s * STAGE + 65536; };
+    auto stage_c = [&](int s) { return smem + s * STAGE; };
+    auto stage_b = [&](int s) { return smem + s * STAGE + 32768; };
+    auto stage_x = [&](int s) { return smem + s * STAGE + 65536; };
 
     if (tid == 0) {
-        mbar_init(&bar[BAR_FULL0], 1);
-        mbar_init(&bar[BAR_FULL1], 1);
-        mbar_init(&bar[BAR_EMPTY0], 1);
-        mbar_init(&bar[BAR_EMPTY1], 1);
-        mbar_init(&bar[BAR_S0], 1);
-        mbar_init(&bar[BAR_S1], 1);
-        mbar_init(&bar[BAR_OPS], 8);
-        mbar_init(&bar[BAR_PRDY], 8);
-        mbar_init(&bar[BAR_ACC], 1);
-        mbar_init(&bar[BAR_DRAIN], 1);
+        for (int b = 0; b < NBAR; ++b) {
+            const bool four = b == OPS_W || b == PRDY || b == OPS_H || b == DS_FREE || b == Y1_FREE;
+            mbar_init(&bar[b], four ? 4 : 1);
+        }
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -248,18 +248,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tm = *sTM;
 
     if (warp == kProducerWarp) {
+        // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
             Cursor cur;
             cur.start(p.cu_chunk, first, last);
             int issued = 0;
             for (int i = 0; i < nblocks; ++i, cur.next()) {
                 const int s = i & 1, u = i >> 1;
-                if (u > 0 && !mbar_wait(&bar[BAR_EMPTY0 + s], (u - 1) & 1)) {
+                if (u > 0 && !mbar_wait(&bar[EMPTY0 + s], (u - 1) & 1)) {
                     report(p.err, SSD_DEVERR_TIMEOUT);
                     break;
                 }
-                uint64_t *full = &bar[BAR_FULL0 + s];
-                mbar_arrive_expect_tx(full, kTxBytes);
+                uint64_t *full = &bar[FULL0 + s];
+                mbar_arrive_expect_tx(full, STAGE);
                 tma_load_3d(stage_c(s), &tmC, 0, g, cur.tb, full);
                 tma_load_3d(stage_c(s) + 16384, &tmC, 64, g, cur.tb, full);
                 tma_load_3d(stage_b(s), &tmB, 0, g, cur.tb, full);
@@ -267,99 +268,105 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(stage_x(s), &tmX, 0, h, cur.tb, full);
                 issued = i + 1;
             }
-            // drain: the copies in flight must land before the CTA may exit
-            for (int i = (issued >= 2 ? issued - 2 : 0); i < issued; ++i)
-                mbar_wait(&bar[BAR_FULL0 + (i & 1)], (i >> 1) & 1);
+            for (int i = (issued >= 2 ? issued - 2 : 0); i < issued; ++i)  // drain
+                mbar_wait(&bar[FULL0 + (i & 1)], (i >> 1) & 1);
         }
     } else if (warp == kMmaWarp) {
+        // ------------------------------------------------ MMA issue -------
         if (lane == 0) {
-            constexpr uint32_t kIdY = idesc_f16(128, 64, 0, 1);  // fp16 operands
+            constexpr uint32_t kIdS = idesc_f16(128, 128, 0, 0);
+            constexpr uint32_t kIdY = idesc_f16(128, 64, 0, 1);
             constexpr uint32_t kIdD = idesc_f16(128, 64, 1, 1);
             const uint32_t aXW = smem_u32(sXW), aH = smem_u32(sH);
-            bool ok = mbar_wait(&bar[BAR_FULL0], 0);
-            int m1_issued = 0;  // blocks whose M1 went out
+            auto issue_m1 = [&](int b) {
+                const int sb = b & 1;
+                const uint32_t aC = smem_u32(stage_c(sb)), aB = smem_u32(stage_b(sb));
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_ss(tm + (sb ? COL_S1 : COL_S0), sw128_desc(aC + ko, 16, 1024), sw128_desc(aB + ko, 16, 1024),
+                           kIdS, k > 0);
+                }
+                mma_commit(&bar[S_RDY0 + sb]);
+            };
+            bool ok = mbar_wait(&bar[FULL0], 0);
+            int m1_issued = 0;
             if (ok) {
                 tc_fence_after();
-                issue_m1(tm + COL_S0, smem_u32(stage_c(0)), smem_u32(stage_b(0)));
-                mma_commit(&bar[BAR_S0]);
+                issue_m1(0);
                 m1_issued = 1;
             }
             for (int i = 0; ok && i < nblocks; ++i) {
                 const int s = i & 1;
                 const uint32_t aC = smem_u32(stage_c(s)), aB = smem_u32(stage_b(s)), aX = smem_u32(stage_x(s));
-                if (!(ok = mbar_wait(&bar[BAR_OPS], i & 1))) break;
+                // M4: dS = B^T (w x) once w x exists and dS of the previous block was read
+                if (!(ok = mbar_wait(&bar[OPS_W], i & 1)) || !(ok = mbar_wait(&bar[DS_FREE], i & 1))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_ss(tm + COL_Y2, sw128_desc(aC + ko, 16, 1024), sw128_desc(aH + 2048 * k, 1024, 1024), kIdY,
-                           k > 0);
-                }
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_ss(tm + COL_DS, sw128_desc(aB + 2048 * k, 16384, 1024), sw128_desc(aXW + 2048 * k, 1024, 1024),
                            kIdD, k > 0);
-                // M2 when P is ready; M1 of the next block after it (its S is needed only
-                // once this block's epilogue is done, and M2 is on the critical path)
-                ok = mbar_wait(&bar[BAR_PRDY], i & 1);
+                mma_commit(&bar[ACC_DS]);
+                // M3: Y2 = C Hprev^T once the state entering the block exists
+                if (!(ok = mbar_wait(&bar[OPS_H], i & 1))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_ss(tm + COL_Y2 + 64 * s, sw128_desc(aC + ko, 16, 1024), sw128_desc(aH + 2048 * k, 1024, 1024),
+                           kIdY, k > 0);
+                }
+                mma_commit(&bar[H_FREE]);
+                // M2 when P is ready (and Y1 was read); M1 of the next block as soon as its tiles land
+                const long long t0 = clock64();
+                for (;;) {
+                    if (m1_issued == i + 1 && i + 1 < nblocks &&
+                        mbar_try_wait(&bar[FULL0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1)) {
+                        tc_fence_after();
+                        issue_m1(i + 1);
+                        ++m1_issued;
+                    }
+                    if (mbar_try_wait(&bar[PRDY], i & 1) && mbar_try_wait(&bar[Y1_FREE], i & 1)) break;
+                    if (clock64() - t0 > 2000000000ll) {
+                        ok = false;
+                        break;
+                    }
+                }
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_ts(tm + COL_Y1, tm + COL_P + 8 * k, sw128_desc(aX + 2048 * k, 1024, 1024), kIdY, k > 0);
-                mma_commit(&bar[BAR_ACC]);
-                mma_commit(&bar[BAR_EMPTY0 + s]);
+                    mma_ts(tm + COL_Y1, tm + (s ? COL_S1 : COL_S0) + 8 * k, sw128_desc(aX + 2048 * k, 1024, 1024), kIdY,
+                           k > 0);
+                mma_commit(&bar[ACC_Y]);
+                mma_commit(&bar[EMPTY0 + s]);
                 if (m1_issued == i + 1 && i + 1 < nblocks) {
-                    const int s1 = (i + 1) & 1;
-                    if (!(ok = mbar_wait(&bar[BAR_FULL0 + s1], ((i + 1) >> 1) & 1))) break;
+                    if (!(ok = mbar_wait(&bar[FULL0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1))) break;
                     tc_fence_after();
-                    issue_m1(tm + (s1 ? COL_S1 : COL_S0), smem_u32(stage_c(s1)), smem_u32(stage_b(s1)));
-                    mma_commit(&bar[BAR_S0 + s1]);
+                    issue_m1(i + 1);
                     ++m1_issued;
                 }
             }
             if (!ok) report(p.err, SSD_DEVERR_TIMEOUT);
-            // drain: one more commit covers every MMA this thread issued
-            mma_commit(&bar[BAR_DRAIN]);
-            mbar_wait(&bar[BAR_DRAIN], 0);
+            mma_commit(&bar[DRAIN]);  // one more commit covers every MMA issued
+            mbar_wait(&bar[DRAIN], 0);
         }
-    } else {
-        // ------------------------------------------------ compute warps ----
-        const int wg = warp >> 2;            // warpgroup: headdim half and column groups
-        const int q = warp & 3;              // warp within the warpgroup
-        const int t = q * 32 + lane;         // TMEM lane / token row / dstate row
+    } else if (warp < 4) {
+        // ------------------------------------ producer warpgroup (P) -------
+        const int q = warp;
+        const int t = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const float Ah = p.A[h];
         const float Dh = p.D ? p.D[h] : 0.f;
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
-        const size_t HPN = (size_t)p.H * kP * kN;
-        float *myF = sF + wg * 128;
-        float *myWT = sWT + wg * 4;
-        float *myC = reinterpret_cast<float *>(smem + OFF_CD) + wg * 256;  // [128] c, then [128] delta
-        float *myD = myC + 128;
-        float st[32];  // state h[p][n = t] for p in [32 wg, 32 wg + 32)
-        {
-            const int32_t is = p.init_slot ? p.init_slot[r] : p.null_id;
-            if (slot_usable(is, p.null_id, p.num_slots, (tid == 0) ? p.err : nullptr)) {
-                const float *src = p.cache + (size_t)is * HPN + (size_t)h * kP * kN + (size_t)(32 * wg) * kN + t;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) st[e] = src[(size_t)e * kN];
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) st[e] = 0.f;
-            }
-        }
-        store_state_half(sH, t, wg, st);
-
         Cursor cur;
         cur.start(p.cu_chunk, first, last);
-        // dt of the next block is loaded one block ahead (its latency hides under this block)
         __nv_bfloat16 dt_next = t < cur.len() ? p.dt[(size_t)(cur.tb + t) * p.H + h] : __float2bfloat16(0.f);
         for (int i = 0; i < nblocks; ++i, cur.next()) {
             const int s = i & 1;
             const uint32_t ph = (i >> 1) & 1;
-            const int tb = cur.tb, L = cur.len();
-            uint8_t *sCs = stage_c(s), *sBs = stage_b(s), *sXs = stage_x(s);
+            const int L = cur.len();
+            uint8_t *sXs = stage_x(s);
             const uint32_t colS = s ? COL_S1 : COL_S0;
             const __nv_bfloat16 dt_cur = dt_next;
             {
@@ -367,11 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nx.next();
                 if (i + 1 < nblocks && t < nx.len()) dt_next = p.dt[(size_t)(nx.tb + t) * p.H + h];
             }
-            // ---- delta, in-block cumsum c_t, factors (each warpgroup on its own)
+            // ---- delta and the in-block cumsum c_t
             float delta = 0.f, a = 0.f;
             if (t < L) {
-                const float v = __bfloat162float(dt_cur) + bias;
-                delta = fast_delta(v, p.dt_softplus, p.dt_min, p.dt_max);
+                delta = fast_delta(__bfloat162float(dt_cur) + bias, p.dt_softplus, p.dt_min, p.dt_max);
                 a = delta * Ah;
             }
             float c = a;
@@ -380,34 +386,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float v = __shfl_up_sync(0xffffffffu, c, off);
                 if (lane >= off) c += v;
             }
-            if (lane == 31) myWT[q] = c;
-            named_bar_sync(1 + wg, 128);
+            if (lane == 31) sWT[q] = c;
+            named_bar_sync(BAR_PG, 128);  // also: every warp is done with the previous block's arrays
             float wt[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) wt[j] = myWT[j];
+            for (int j = 0; j < 4; ++j) wt[j] = sWT[j];
             float prefix = 0.f, own = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (j < q) prefix += wt[j];
                 if (j == q) own = wt[j];
             }
-            c += prefix;                                  // c_t
+            c += prefix;
             const float c_last = wt[0] + wt[1] + wt[2] + wt[3];
-            myF[t] = __expf(prefix + own - c) * delta;     // column factor of column t
-            myC[t] = c;
-            myD[t] = delta;
-            const float w_x = __expf(c_last - c) * delta;  // state-update weight of token t
-            const float e_row = __expf(c);                 // carried-state factor of row t
-            const float decay = __expf(c_last);
+            sF[t] = __expf(prefix + own - c) * delta;  // column factor of column t
+            sCc[t] = c;
+            sDl[t] = delta;
+            sE[(i % kRing) * 128 + t] = __expf(c);     // carried-state factor of row t (consumer)
+            if (t == 0) sDec[i % kRing] = __expf(c_last);
+            const float w_x = __expf(c_last - c) * delta;
 
-            // ---- tiles landed: w x and x -> fp16 (this warpgroup's half of row t)
-            bool ok = warp_wait(&bar[BAR_FULL0 + s], ph);
-            if (!named_bar_and(BAR_VOTE, kCompute, ok)) {
-                if (tid == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+            // ---- w x (fp16) into the M4 operand once M4 of the previous block is done; x -> fp16
+            bool ok = warp_wait(&bar[FULL0 + s], ph);
+            if (ok && i > 0) ok = warp_wait(&bar[ACC_DS], (i - 1) & 1);
+            if (!named_bar_and(BAR_PG, 128, ok)) {
+                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
             }
 #pragma unroll
-            for (int cc = 4 * wg; cc < 4 * wg + 4; ++cc) {
+            for (int cc = 0; cc < 8; ++cc) {
                 const uint4 v = *reinterpret_cast<const uint4 *>(sXs + sw128_offset(t, cc));
                 uint4 xw;
                 xw.x = pack_f16_sat(w_x * __uint_as_float(v.x << 16), w_x * __uint_as_float(v.x & 0xFFFF0000u));
@@ -417,88 +424,154 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
                 *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = bf16x8_to_f16x8(v);
             }
-            // ---- S ready
-            ok = warp_wait(&bar[BAR_S0 + s], ph);
-            if (!named_bar_and(BAR_VOTE, kCompute, ok)) {
-                if (tid == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[OPS_W]);
+
+            // ---- S ready: P pass, S (fp32) -> P (fp16) over the same columns
+            ok = warp_wait(&bar[S_RDY0 + s], ph);
+            if (!named_bar_and(BAR_PG, 128, ok)) {
+                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            fence_proxy_async_smem();  // w x, x and the state tile -> async proxy
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[BAR_OPS]);
-
-            // ---- P pass: S (fp32) -> P (fp16) in TMEM, column groups {wg, wg + 2}
+            // Group j of P goes over columns [16j, 16j+16), which hold S groups <= j that this
+            // warp has already read.  The loops stay rolled: the four warp roles run different
+            // code, and unrolled copies of these bodies overflow the instruction cache.
+            float gend = 0.f;
+#pragma unroll 1
+            for (int j = 0; j < q; ++j) {  // groups below the diagonal
+                uint32_t v[32], pk[16];
+                tmem_ld32(tm + lane_base + colS + 32 * j, v);
+                gend += j == 0 ? wt[0] : (j == 1 ? wt[1] : wt[2]);
+                const float R = __expf(c - gend);
+                const float4 *f4 = reinterpret_cast<const float4 *>(sF + 32 * j);
+                tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const int j = wg + 2 * jj;
-                uint32_t pk[16];
-                if (j < q) {
-                    uint32_t v[32];
-                    tmem_ld32(tm + lane_base + colS + 32 * j, v);
-                    tmem_ld_wait();
-                    float gend = 0.f;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (u <= j) gend += wt[u];
-                    const float R = __expf(c - gend);
-                    const float4 *f4 = reinterpret_cast<const float4 *>(myF + 32 * j);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const float4 f = f4[u];
-                        pk[2 * u] = pack_f16_sat(__uint_as_float(v[4 * u]) * f.x * R, __uint_as_float(v[4 * u + 1]) * f.y * R);
-                        pk[2 * u + 1] = pack_f16_sat(__uint_as_float(v[4 * u + 2]) * f.z * R,
-                                                     __uint_as_float(v[4 * u + 3]) * f.w * R);
-                    }
-                } else if (j == q) {
-                    // diagonal group: one exponential per element, branch-free (c, delta of the
-                    // columns by broadcast from shared memory; the mask by select)
-                    uint32_t v[32];
-                    tmem_ld32(tm + lane_base + colS + 32 * j, v);
-                    tmem_ld_wait();
-                    const float4 *c4 = reinterpret_cast<const float4 *>(myC + 32 * j);
-                    const float4 *d4 = reinterpret_cast<const float4 *>(myD + 32 * j);
-#pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
-                        const float4 cs = c4[u4], ds = d4[u4];
-                        const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, dv[4] = {ds.x, ds.y, ds.z, ds.w};
-                        float pv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int u = 4 * u4 + e;
-                            const float ex = __expf(fminf(c - cv[e], 0.f));
-                            const float val = __uint_as_float(v[u]) * ex * dv[e];
-                            pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
-                        }
-                        pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
-                        pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) pk[u] = 0u;
+                for (int u = 0; u < 8; ++u) {
+                    const float4 f = f4[u];
+                    pk[2 * u] = pack_f16_sat(__uint_as_float(v[4 * u]) * f.x * R, __uint_as_float(v[4 * u + 1]) * f.y * R);
+                    pk[2 * u + 1] =
+                        pack_f16_sat(__uint_as_float(v[4 * u + 2]) * f.z * R, __uint_as_float(v[4 * u + 3]) * f.w * R);
                 }
-                tmem_st16(tm + lane_base + COL_P + 16 * j, pk);
+                tmem_st16(tm + lane_base + colS + 16 * j, pk);
+            }
+            {  // the diagonal group j = q: one exponential per element, the mask by select
+                uint32_t v[32], pk[16];
+                tmem_ld32(tm + lane_base + colS + 32 * q, v);
+                const float4 *c4 = reinterpret_cast<const float4 *>(sCc + 32 * q);
+                const float4 *d4 = reinterpret_cast<const float4 *>(sDl + 32 * q);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const float4 cs = c4[u4], ds = d4[u4];
+                    const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, dv[4] = {ds.x, ds.y, ds.z, ds.w};
+                    float pv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int u = 4 * u4 + e;
+                        const float ex = __expf(fminf(c - cv[e], 0.f));
+                        const float val = __uint_as_float(v[u]) * ex * dv[e];
+                        pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
+                    }
+                    pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
+                    pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
+                }
+                tmem_st16(tm + lane_base + colS + 16 * q, pk);
+            }
+            {
+                uint32_t zero[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) zero[u] = 0u;
+#pragma unroll 1
+                for (int j = q + 1; j < 4; ++j) tmem_st16(tm + lane_base + colS + 16 * j, zero);  // above the diagonal
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[BAR_PRDY]);
-
-            // ---- accumulators ready
-            ok = warp_wait(&bar[BAR_ACC], i & 1);
-            if (!named_bar_and(BAR_VOTE, kCompute, ok)) {
-                if (tid == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+            if (lane == 0) mbar_arrive(&bar[PRDY]);
+        }
+    } else {
+        // ------------------------------------ consumer warpgroup (E) -------
+        const int q = warp - 4;
+        const int t = q * 32 + lane;  // TMEM lane: token row t of Y, dstate row t of dS and the state
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const size_t HPN = (size_t)p.H * kP * kN;
+        float st[kP];  // state h[p][n = t]
+        {
+            const int32_t is = p.init_slot ? p.init_slot[r] : p.null_id;
+            if (slot_usable(is, p.null_id, p.num_slots, (t == 0) ? p.err : nullptr)) {
+                const float *src = p.cache + (size_t)is * HPN + (size_t)h * kP * kN + t;
+#pragma unroll
+                for (int e = 0; e < kP; ++e) st[e] = src[(size_t)e * kN];
+            } else {
+#pragma unroll
+                for (int e = 0; e < kP; ++e) st[e] = 0.f;
+            }
+        }
+        store_state_row(sH, t, st);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&bar[OPS_H]);    // the state entering block 0
+            mbar_arrive(&bar[DS_FREE]);  // dS and Y1 start out free
+            mbar_arrive(&bar[Y1_FREE]);
+        }
+        Cursor cur;
+        cur.start(p.cu_chunk, first, last);
+        for (int i = 0; i < nblocks; ++i, cur.next()) {
+            const int s = i & 1;
+            const int tb = cur.tb, L = cur.len();
+            // ---- dS: the state after this block, then the fp16 state for the next block's M3
+            bool ok = warp_wait(&bar[ACC_DS], i & 1);
+            if (!named_bar_and(BAR_CG, 128, ok)) {
+                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            {
-                uint32_t d[32], y1[32], y2[32];
-                tmem_ld32(tm + lane_base + COL_DS + 32 * wg, d);
-                tmem_ld32(tm + lane_base + COL_Y1 + 32 * wg, y1);
-                tmem_ld32(tm + lane_base + COL_Y2 + 32 * wg, y2);
+            const float decay = sDec[i % kRing];
+            const float e_row = sE[(i % kRing) * 128 + t];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t d[32];
+                tmem_ld32(tm + lane_base + COL_DS + 32 * half, d);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) st[e] = fmaf(decay, st[e], __uint_as_float(d[e]));
+                for (int e = 0; e < 32; ++e) st[32 * half + e] = fmaf(decay, st[32 * half + e], __uint_as_float(d[e]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[DS_FREE]);  // M4 of the next block may overwrite dS
+            ok = warp_wait(&bar[H_FREE], i & 1);          // M3 of this block has read the state tile
+            if (!named_bar_and(BAR_CG, 128, ok)) {
+                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+                break;
+            }
+            store_state_row(sH, t, st);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[OPS_H]);  // the state entering the next block
+            if (cur.ends_chunk()) {
+                const int32_t cs = p.chunk_slot ? p.chunk_slot[cur.k] : p.null_id;
+                if (slot_usable(cs, p.null_id, p.num_slots, (t == 0) ? p.err : nullptr)) {
+                    float *dst = p.cache + (size_t)cs * HPN + (size_t)h * kP * kN + t;
+#pragma unroll
+                    for (int e = 0; e < kP; ++e) dst[(size_t)e * kN] = st[e];
+                }
+            }
+            // ---- y = Y1 + exp(c_t) Y2
+            ok = warp_wait(&bar[ACC_Y], i & 1);
+            if (!named_bar_and(BAR_CG, 128, ok)) {
+                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t y1[32], y2[32];
+                tmem_ld32(tm + lane_base + COL_Y1 + 32 * half, y1);
+                tmem_ld32(tm + lane_base + COL_Y2 + 64 * s + 32 * half, y2);
+                tmem_ld_wait();
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint4 v;
@@ -509,28 +582,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         vv[u] = pack_bf16(fmaf(e_row, __uint_as_float(y2[e]), __uint_as_float(y1[e])),
                                           fmaf(e_row, __uint_as_float(y2[e + 1]), __uint_as_float(y1[e + 1])));
                     }
-                    *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, 4 * wg + cc)) = v;
+                    *reinterpret_cast<uint4 *>(sY + sw128_offset(t, 4 * half + cc)) = v;
                 }
             }
             tc_fence_before();
-            store_state_half(sH, t, wg, st);
-            if (cur.ends_chunk()) {
-                const int32_t cs = p.chunk_slot ? p.chunk_slot[cur.k] : p.null_id;
-                if (slot_usable(cs, p.null_id, p.num_slots, (tid == 0) ? p.err : nullptr)) {
-                    float *dst = p.cache + (size_t)cs * HPN + (size_t)h * kP * kN + (size_t)(32 * wg) * kN + t;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[Y1_FREE]);  // M2 of the next block may overwrite Y1
+            named_bar_sync(BAR_CG, 128);  // y tile staged
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) dst[(size_t)e * kN] = st[e];
-                }
-            }
-            named_bar_sync(BAR_VOTE, kCompute);  // y tile staged
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const int row = rr * 32 + (tid >> 3), cc = tid & 7;
+            for (int rr = 0; rr < 8; ++rr) {
+                const int row = rr * 16 + (t >> 3), cc = t & 7;
                 if (row < L) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(sXW + sw128_offset(row, cc));
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sY + sw128_offset(row, cc));
                     *reinterpret_cast<uint4 *>(p.y + ((size_t)(tb + row) * p.H + h) * kP + 8 * cc) = v;
                 }
             }
+            named_bar_sync(BAR_CG, 128);  // the staging tile may be reused
         }
     }
     tc_fence_before();
