@@ -142,16 +142,19 @@ __device__ __forceinline__ float fast_delta(float v, int dt_softplus, float lo, 
 }
 
 // Walks the blocks of one sequence: chunks [first, last], each cut into
-// blocks of at most kL tokens that never cross a chunk end.
+// blocks of at most kL tokens that never cross a chunk end.  The end of the
+// following chunk is loaded one chunk ahead (from a clamped index, so the
+// load is unconditional), so moving to the next chunk never waits on memory.
 struct Cursor {
     const int32_t *cu_chunk;
-    int k, last, tb, ce;
+    int k, last, tb, ce, ce_next;
     __device__ void start(const int32_t *cc, int first, int last_) {
         cu_chunk = cc;
         k = first;
         last = last_;
         tb = cc[first];
         ce = cc[first + 1];
+        ce_next = cc[min(first + 2, last_ + 1)];
     }
     __device__ int len() const { return min(kL, ce - tb); }
     __device__ bool ends_chunk() const { return tb + len() == ce; }
@@ -159,7 +162,8 @@ struct Cursor {
         tb += len();
         if (tb == ce && k < last) {
             ++k;
-            ce = cu_chunk[k + 1];
+            ce = ce_next;
+            ce_next = cu_chunk[min(k + 2, last + 1)];
         }
     }
 };
@@ -361,7 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
         Cursor cur;
         cur.start(p.cu_chunk, first, last);
-        __nv_bfloat16 dt_next = t < cur.len() ? p.dt[(size_t)(cur.tb + t) * p.H + h] : __float2bfloat16(0.f);
+        // dt of row t of the next block, loaded a block ahead from a clamped (always valid)
+        // token; rows past the block's end are masked where it is used
+        __nv_bfloat16 dt_next = p.dt[(size_t)min(cur.tb + t, p.T - 1) * p.H + h];
         for (int i = 0; i < nblocks; ++i, cur.next()) {
             const int s = i & 1;
             const uint32_t ph = (i >> 1) & 1;
@@ -369,11 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *sXs = stage_x(s);
             const uint32_t colS = s ? COL_S1 : COL_S0;
             const __nv_bfloat16 dt_cur = dt_next;
-            {
-                Cursor nx = cur;
-                nx.next();
-                if (i + 1 < nblocks && t < nx.len()) dt_next = p.dt[(size_t)(nx.tb + t) * p.H + h];
-            }
+            dt_next = p.dt[(size_t)min(cur.tb + L + t, p.T - 1) * p.H + h];  // blocks of a sequence are contiguous
             // ---- delta and the in-block cumsum c_t
             float delta = 0.f, a = 0.f;
             if (t < L) {
@@ -519,6 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         Cursor cur;
         cur.start(p.cu_chunk, first, last);
+        // cache slot of the current chunk's end state, loaded a chunk ahead of its use
+        int32_t cs = p.chunk_slot ? p.chunk_slot[first] : p.null_id;
         for (int i = 0; i < nblocks; ++i, cur.next()) {
             const int s = i & 1;
             const int tb = cur.tb, L = cur.len();
@@ -552,12 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[OPS_H]);  // the state entering the next block
             if (cur.ends_chunk()) {
-                const int32_t cs = p.chunk_slot ? p.chunk_slot[cur.k] : p.null_id;
                 if (slot_usable(cs, p.null_id, p.num_slots, (t == 0) ? p.err : nullptr)) {
                     float *dst = p.cache + (size_t)cs * HPN + (size_t)h * kP * kN + t;
 #pragma unroll
                     for (int e = 0; e < kP; ++e) dst[(size_t)e * kN] = st[e];
                 }
+                if (p.chunk_slot) cs = p.chunk_slot[min(cur.k + 1, last)];
             }
             // ---- y = Y1 + exp(c_t) Y2
             ok = warp_wait(&bar[ACC_Y], i & 1);
