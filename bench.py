@@ -220,12 +220,30 @@ def _barrier(dist_on):
         torch.distributed.barrier()
 
 
-def _max_over_ranks(v, dist_on, dev):
+def _reduce_over_ranks(v, dist_on, dev, op):
     if not dist_on:
         return v
     t = torch.tensor([v], dtype=torch.float64, device=dev)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(t, op=op)
     return float(t.item())
+
+
+def _max_over_ranks(v, dist_on, dev):
+    """Slowest rank's value (timings: the job ends when the last rank does)."""
+    return _reduce_over_ranks(v, dist_on, dev, torch.distributed.ReduceOp.MAX if dist_on else None)
+
+
+def _sum_over_ranks(v, dist_on, dev):
+    """Total over ranks (units of work every rank processed)."""
+    return _reduce_over_ranks(v, dist_on, dev, torch.distributed.ReduceOp.SUM if dist_on else None)
+
+
+def job_rate(local_units, local_ms, steps, dist_on, dev):
+    """Whole-job throughput of independent replicas: the units all ranks
+    processed over the slowest rank's time.  Returns (units/s, ms per step)."""
+    units = _sum_over_ranks(float(local_units), dist_on, dev)
+    ms = _max_over_ranks(float(local_ms), dist_on, dev)
+    return units / (ms / steps * 1e-3), ms / steps
 
 
 def gpu_arm(args, rank, world, dist_on):
@@ -256,12 +274,12 @@ def gpu_arm(args, rank, world, dist_on):
         t1.record()
         torch.cuda.synchronize()
         _barrier(dist_on)
-    elapsed_ms = _max_over_ranks(t0.elapsed_time(t1), dist_on, dev)
+    value, ms_step = job_rate(T + R, t0.elapsed_time(t1), args.steps, dist_on, dev)
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
 
     # end to end: inputs from pinned host memory, y back to host, every step
-    e2e_ms, h2d, d2h = None, 0, 0
+    e2e_value, e2e_ms, h2d, d2h = None, None, 0, 0
     if not args.no_e2e:
         host, h2d, d2h = st.host_buffers()
         st.run(host=host)
@@ -274,18 +292,16 @@ def gpu_arm(args, rank, world, dist_on):
             st.run(host=host)
         e1.record()
         torch.cuda.synchronize()
-        e2e_ms = _max_over_ranks(e0.elapsed_time(e1), dist_on, dev)
+        e2e_value, e2e_ms = job_rate(T + R, e0.elapsed_time(e1), args.steps, dist_on, dev)
 
     if rank != 0:
         return None
-    ms_step = elapsed_ms / args.steps
-    units = (T + R) * world
     hbm, peak_kind = _peaks()
     pre_mean = statistics.mean(pre_ms)
     dec_mean = statistics.mean(dec_ms) if R > 0 else 0.0
     achieved = pre_bytes / (pre_mean * 1e-3) / 1e9
     line = {
-        "metric": METRIC, "value": units / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded randn tokens, -exp(U(0,2)) A, U(-4,-1) dt_bias)",
@@ -301,7 +317,7 @@ def gpu_arm(args, rank, world, dist_on):
                      "peak_source": peak_kind, "traffic": None,
                      "units": "prefill algorithmic bytes per call / mean call time (CUDA events)"},
         "clocks": clk.summary(),
-        "e2e": None if e2e_ms is None else {"value": units / (e2e_ms / args.steps * 1e-3), "unit": UNIT,
+        "e2e": None if e2e_ms is None else {"value": e2e_value, "unit": UNIT,
                                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (st.prefill_kernels + (1 if R else 0)) * args.steps,
     }
