@@ -77,22 +77,26 @@ constexpr uint32_t COL_Y1 = 256;   // P X
 constexpr uint32_t COL_Y2 = 320;   // C Hprev^T, even / odd blocks at +0 / +64
 constexpr uint32_t COL_DS = 448;   // B^T (w x)
 // shared memory (offsets from the 1024-aligned dynamic base)
-constexpr uint32_t STAGE = 81920;            // C 32 KB | B 32 KB | x 16 KB
-constexpr uint32_t OFF_XW = 2 * STAGE;       // w x (fp16)
+constexpr uint32_t CB_STAGE = 65536;         // C 32 KB | B 32 KB (fp16)
+constexpr uint32_t X_STAGE = 16384;          // x tile; then its fp16 copy; then y staging
+constexpr int kCbStages = 2, kXStages = 3;
+constexpr uint32_t OFF_X = kCbStages * CB_STAGE;
+constexpr uint32_t OFF_XW = OFF_X + kXStages * X_STAGE;  // w x (fp16)
 constexpr uint32_t OFF_H = OFF_XW + 16384;   // fp16 state entering the block
-constexpr uint32_t OFF_Y = OFF_H + 16384;    // y staging (bf16)
-constexpr uint32_t OFF_F = OFF_Y + 16384;    // column factors [128]
+constexpr uint32_t OFF_F = OFF_H + 16384;    // column factors [128]
 constexpr uint32_t OFF_CD = OFF_F + 512;     // c_t and delta_t [2][128]
 constexpr uint32_t OFF_E = OFF_CD + 1024;    // exp(c_t) per block, ring of 4 [4][128]
 constexpr uint32_t OFF_DEC = OFF_E + 2048;   // exp(c_L) per block, ring of 4
 constexpr uint32_t OFF_WT = OFF_DEC + 16;    // warp sums of delta*A [4]
 constexpr uint32_t OFF_TM = OFF_WT + 16;     // TMEM base address
 constexpr uint32_t OFF_BAR = OFF_TM + 16;    // mbarriers
-constexpr uint32_t kSmemBytes = OFF_BAR + 16 * 8;
+constexpr uint32_t kSmemBytes = OFF_BAR + 24 * 8;
 constexpr int kRing = 4;
 
 enum {
-    FULL0 = 0, FULL1, EMPTY0, EMPTY1, S_RDY0, S_RDY1,  // tiles and S, per stage
+    FULL_CB0 = 0, FULL_CB1, EMPTY_CB0, EMPTY_CB1,      // C/B ring: freed once M3 of the block is done
+    FULL_X0, FULL_X1, FULL_X2, EMPTY_X0, EMPTY_X1, EMPTY_X2,  // x ring: freed after y (EMPTY: 4 arrivals)
+    S_RDY0, S_RDY1,                                    // S of the block, per S buffer
     OPS_W,     // producer wg: w x and fp16 x of the block are in smem          (4 arrivals)
     PRDY,      // producer wg: P of the block is in TMEM                        (4)
     OPS_H,     // consumer wg: fp16 state entering the block is in smem         (4)
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) report(p.err, SSD_DEVERR_INTERNAL);
         return;
     }
-    uint8_t *sXW = smem + OFF_XW, *sH = smem + OFF_H, *sY = smem + OFF_Y;
+    uint8_t *sXW = smem + OFF_XW, *sH = smem + OFF_H;
     float *sF = reinterpret_cast<float *>(smem + OFF_F);
     float *sCc = reinterpret_cast<float *>(smem + OFF_CD);
     float *sDl = sCc + 128;
@@ -226,13 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sWT = reinterpret_cast<float *>(smem + OFF_WT);
     uint32_t *sTM = reinterpret_cast<uint32_t *>(smem + OFF_TM);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    auto stage_c = [&](int s) { return smem + s * STAGE; };
-    auto stage_b = [&](int s) { return smem + s * STAGE + 32768; };
-    auto stage_x = [&](int s) { return smem + s * STAGE + 65536; };
+    auto stage_c = [&](int s) { return smem + s * CB_STAGE; };
+    auto stage_b = [&](int s) { return smem + s * CB_STAGE + 32768; };
+    auto stage_x = [&](int b) { return smem + OFF_X + (b % kXStages) * X_STAGE; };  // by block index
 
     if (tid == 0) {
         for (int b = 0; b < NBAR; ++b) {
-            const bool four = b == OPS_W || b == PRDY || b == OPS_H || b == DS_FREE || b == Y1_FREE;
+            const bool four = b == OPS_W || b == PRDY || b == OPS_H || b == DS_FREE || b == Y1_FREE ||
+                              (b >= EMPTY_X0 && b <= EMPTY_X2);
             mbar_init(&bar[b], four ? 4 : 1);
         }
         fence_mbar_init();
@@ -254,26 +259,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
-            Cursor cur;
-            cur.start(p.cu_chunk, first, last);
-            int issued = 0;
-            for (int i = 0; i < nblocks; ++i, cur.next()) {
-                const int s = i & 1, u = i >> 1;
-                if (u > 0 && !mbar_wait(&bar[EMPTY0 + s], (u - 1) & 1)) {
+            // Two rings, each refilled as soon as its slot frees: C/B tiles once M3 of the
+            // block two back is done, x tiles once y of the block three back is out.
+            Cursor ccb, cx;
+            ccb.start(p.cu_chunk, first, last);
+            cx.start(p.cu_chunk, first, last);
+            int ncb = 0, nx = 0;
+            long long t_prog = clock64();
+            while (ncb < nblocks || nx < nblocks) {
+                bool prog = false;
+                if (ncb < nblocks) {
+                    const int s = ncb & 1;
+                    if (ncb < kCbStages || mbar_test(&bar[EMPTY_CB0 + s], ((ncb >> 1) - 1) & 1)) {
+                        uint64_t *full = &bar[FULL_CB0 + s];
+                        mbar_arrive_expect_tx(full, CB_STAGE);
+                        tma_load_3d(stage_c(s), &tmC, 0, g, ccb.tb, full);
+                        tma_load_3d(stage_c(s) + 16384, &tmC, 64, g, ccb.tb, full);
+                        tma_load_3d(stage_b(s), &tmB, 0, g, ccb.tb, full);
+                        tma_load_3d(stage_b(s) + 16384, &tmB, 64, g, ccb.tb, full);
+                        ccb.next();
+                        ++ncb;
+                        prog = true;
+                    }
+                }
+                if (nx < nblocks) {
+                    if (nx < kXStages || mbar_test(&bar[EMPTY_X0 + nx % kXStages], (nx / kXStages - 1) & 1)) {
+                        uint64_t *full = &bar[FULL_X0 + nx % kXStages];
+                        mbar_arrive_expect_tx(full, X_STAGE);
+                        tma_load_3d(stage_x(nx), &tmX, 0, h, cx.tb, full);
+                        cx.next();
+                        ++nx;
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    t_prog = clock64();
+                } else if (clock64() - t_prog > 2000000000ll) {
                     report(p.err, SSD_DEVERR_TIMEOUT);
                     break;
+                } else if (ncb < nblocks) {
+                    // nothing to issue: the hardware suspends this thread until the next C/B stage
+                    // frees, or a short while passes so the x ring is looked at again
+                    mbar_try_wait_sleep(&bar[EMPTY_CB0 + (ncb & 1)], ((ncb >> 1) - 1) & 1, 300);
+                } else {
+                    mbar_try_wait_sleep(&bar[EMPTY_X0 + nx % kXStages], (nx / kXStages - 1) & 1, 300);
                 }
-                uint64_t *full = &bar[FULL0 + s];
-                mbar_arrive_expect_tx(full, STAGE);
-                tma_load_3d(stage_c(s), &tmC, 0, g, cur.tb, full);
-                tma_load_3d(stage_c(s) + 16384, &tmC, 64, g, cur.tb, full);
-                tma_load_3d(stage_b(s), &tmB, 0, g, cur.tb, full);
-                tma_load_3d(stage_b(s) + 16384, &tmB, 64, g, cur.tb, full);
-                tma_load_3d(stage_x(s), &tmX, 0, h, cur.tb, full);
-                issued = i + 1;
             }
-            for (int i = (issued >= 2 ? issued - 2 : 0); i < issued; ++i)  // drain
-                mbar_wait(&bar[FULL0 + (i & 1)], (i >> 1) & 1);
+            // drain: no copy may still be landing when the CTA exits
+            for (int i = max(ncb - kCbStages, 0); i < ncb; ++i) mbar_wait(&bar[FULL_CB0 + (i & 1)], (i >> 1) & 1);
+            for (int i = max(nx - kXStages, 0); i < nx; ++i) mbar_wait(&bar[FULL_X0 + i % kXStages], (i / kXStages) & 1);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issue -------
@@ -293,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&bar[S_RDY0 + sb]);
             };
-            bool ok = mbar_wait(&bar[FULL0], 0);
+            bool ok = mbar_wait(&bar[FULL_CB0], 0);
             int m1_issued = 0;
             if (ok) {
                 tc_fence_after();
@@ -302,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int i = 0; ok && i < nblocks; ++i) {
                 const int s = i & 1;
-                const uint32_t aC = smem_u32(stage_c(s)), aB = smem_u32(stage_b(s)), aX = smem_u32(stage_x(s));
+                const uint32_t aC = smem_u32(stage_c(s)), aB = smem_u32(stage_b(s)), aX = smem_u32(stage_x(i));
                 // M4: dS = B^T (w x) once w x exists and dS of the previous block was read
                 if (!(ok = mbar_wait(&bar[OPS_W], i & 1)) || !(ok = mbar_wait(&bar[DS_FREE], i & 1))) break;
                 tc_fence_after();
@@ -321,11 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                            kIdY, k > 0);
                 }
                 mma_commit(&bar[H_FREE]);
+                mma_commit(&bar[EMPTY_CB0 + s]);  // M1, M4 and M3 of the block have read its C/B stage
                 // M2 when P is ready (and Y1 was read); M1 of the next block as soon as its tiles land
                 const long long t0 = clock64();
                 for (;;) {
                     if (m1_issued == i + 1 && i + 1 < nblocks &&
-                        mbar_try_wait(&bar[FULL0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1)) {
+                        mbar_try_wait(&bar[FULL_CB0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1)) {
                         tc_fence_after();
                         issue_m1(i + 1);
                         ++m1_issued;
@@ -343,9 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ts(tm + COL_Y1, tm + (s ? COL_S1 : COL_S0) + 8 * k, sw128_desc(aX + 2048 * k, 1024, 1024), kIdY,
                            k > 0);
                 mma_commit(&bar[ACC_Y]);
-                mma_commit(&bar[EMPTY0 + s]);
                 if (m1_issued == i + 1 && i + 1 < nblocks) {
-                    if (!(ok = mbar_wait(&bar[FULL0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1))) break;
+                    if (!(ok = mbar_wait(&bar[FULL_CB0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1))) break;
                     tc_fence_after();
                     issue_m1(i + 1);
                     ++m1_issued;
@@ -372,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = i & 1;
             const uint32_t ph = (i >> 1) & 1;
             const int L = cur.len();
-            uint8_t *sXs = stage_x(s);
+            uint8_t *sXs = stage_x(i);
             const uint32_t colS = s ? COL_S1 : COL_S0;
             const __nv_bfloat16 dt_cur = dt_next;
             dt_next = p.dt[(size_t)min(cur.tb + L + t, p.T - 1) * p.H + h];  // blocks of a sequence are contiguous
@@ -406,10 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             sDl[t] = delta;
             sE[(i % kRing) * 128 + t] = __expf(c);     // carried-state factor of row t (consumer)
             if (t == 0) sDec[i % kRing] = __expf(c_last);
-            const float w_x = __expf(c_last - c) * delta;
+            // w_t as fp16x2, for w x computed as an fp16 product of the (exactly) converted x
+            const uint32_t w2 = pack_f16_sat(__expf(c_last - c) * delta, __expf(c_last - c) * delta);
 
             // ---- w x (fp16) into the M4 operand once M4 of the previous block is done; x -> fp16
-            bool ok = warp_wait(&bar[FULL0 + s], ph);
+            bool ok = warp_wait(&bar[FULL_X0 + i % kXStages], (i / kXStages) & 1);
             if (ok && i > 0) ok = warp_wait(&bar[ACC_DS], (i - 1) & 1);
             if (!named_bar_and(BAR_PG, 128, ok)) {
                 if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
@@ -417,14 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(sXs + sw128_offset(t, cc));
-                uint4 xw;
-                xw.x = pack_f16_sat(w_x * __uint_as_float(v.x << 16), w_x * __uint_as_float(v.x & 0xFFFF0000u));
-                xw.y = pack_f16_sat(w_x * __uint_as_float(v.y << 16), w_x * __uint_as_float(v.y & 0xFFFF0000u));
-                xw.z = pack_f16_sat(w_x * __uint_as_float(v.z << 16), w_x * __uint_as_float(v.z & 0xFFFF0000u));
-                xw.w = pack_f16_sat(w_x * __uint_as_float(v.w << 16), w_x * __uint_as_float(v.w & 0xFFFF0000u));
+                const uint4 xh = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(sXs + sw128_offset(t, cc)));
+                const uint4 xw = make_uint4(hmul2_u32(xh.x, w2), hmul2_u32(xh.y, w2), hmul2_u32(xh.z, w2),
+                                            hmul2_u32(xh.w, w2));
                 *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
-                *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = bf16x8_to_f16x8(v);
+                *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = xh;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -535,13 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float decay = sDec[i % kRing];
             const float e_row = sE[(i % kRing) * 128 + t];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t d[32];
-                tmem_ld32(tm + lane_base + COL_DS + 32 * half, d);
+            {
+                uint32_t d[64];
+                tmem_ld64(tm + lane_base + COL_DS, d);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) st[32 * half + e] = fmaf(decay, st[32 * half + e], __uint_as_float(d[e]));
+                for (int e = 0; e < 64; ++e) st[e] = fmaf(decay, st[e], __uint_as_float(d[e]));
             }
             tc_fence_before();
             __syncwarp();
@@ -570,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            uint8_t *sY = stage_x(i);  // y staging: the block's x slot, which M2 has finished with
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 uint32_t y1[32], y2[32];
@@ -601,7 +633,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(p.y + ((size_t)(tb + row) * p.H + h) * kP + 8 * cc) = v;
                 }
             }
-            named_bar_sync(BAR_CG, 128);  // the staging tile may be reused
+            fence_proxy_async_smem();  // this warp's reads of the slot come before the next TMA write
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[EMPTY_X0 + i % kXStages]);
         }
     }
     tc_fence_before();
