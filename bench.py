@@ -43,6 +43,11 @@ WORKLOADS = {
                            num_decodes=0, chunk_size=256, nheads=128, headdim=64, dstate=128, ngroups=8,
                            cache_slots=512, token_dtype="bf16", state_dtype="fp32",
                            l2="inputs larger than L2 (no flush)"),
+    # the decode kernel at the long batch's request count, on a smaller cache (about 4 GB) for captures
+    "decode_384": dict(workload="384 single-token decodes on a 1024-slot cache, one 256-token prefill (profiling size)",
+                       num_prefills=1, prefill_len=256, num_decodes=384, chunk_size=256, nheads=128, headdim=64,
+                       dstate=128, ngroups=8, cache_slots=1024, token_dtype="bf16", state_dtype="fp32",
+                       l2="state reads larger than L2 (no flush)"),
 }
 WORKLOAD = WORKLOADS["long_mixed"]
 
@@ -57,6 +62,19 @@ def _peaks():
 
 
 # ------------------------------------------------------------- byte counts --
+
+# DRAM traffic of one prefill call, from one ncu capture of the fused kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum = 3.472 GB for 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256), scaled
+# by tokens (x, y, B/C and one state per chunk all grow with them), plus the B/C pre-conversion, which
+# streams 2*T*G*N*2 bytes in and as many out.  Only for that head configuration and kernel version.
+FUSED_TRAFFIC_PER_TOKEN = 3.472e9 / 65536
+
+
+def prefill_traffic(T, H, P, N, G):
+    if (H, P, N, G) != (128, 64, 128, 8):
+        return None
+    return FUSED_TRAFFIC_PER_TOKEN * T + 4.0 * T * G * N * 2
+
 
 def prefill_bytes(T, K, H, P, N, G, elt, init_reads=0):
     """Algorithmic HBM bytes of one prefill call: x in, y out, dt, B, C per
@@ -314,7 +332,8 @@ def gpu_arm(args, rank, world, dist_on):
                    "hbm_frac": dec_bytes / (dec_mean * 1e-3) / 1e9 / hbm if R else None},
         "roofline": {"kernel": "ssd_prefill_varlen (%d kernels)" % st.prefill_kernels, "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": peak_kind, "traffic": None,
+                     "traffic": prefill_traffic(T, H, P, N, G),
+                     "peak_source": peak_kind,
                      "units": "prefill algorithmic bytes per call / mean call time (CUDA events)"},
         "clocks": clk.summary(),
         "e2e": None if e2e_ms is None else {"value": e2e_value, "unit": UNIT,
