@@ -106,16 +106,31 @@ def delta(dt, bias, dt_softplus=True, dt_limit=(0.0, math.inf)):
                                       float(dt_limit[0]), float(dt_limit[1]))
 
 
+def silu(z):
+    """silu(z) = z * sigmoid(z), in fp64, with sigmoid(z) = 1 / (1 + e) for
+    z >= 0 and e / (1 + e) for z < 0, e = exp(-|z|): neither branch
+    overflows, and neither subtracts nearly equal numbers.
+
+    The output gate: the chunk-scan call of "[vllm] vLLM Mamba2 SSD 커널 웜업"
+    ("mamba_mixer2.py 변경 사항 (핵심)") takes an optional z (None in the
+    warm-up); as in Mamba2, a gated output is y * silu(z) elementwise.
+    """
+    z = _f64(z)
+    e = np.exp(-np.abs(z))
+    return z * np.where(z >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
 def ssd_prefill(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens=None, D=None, dt_bias=None,
                 initial_states=None, has_initial_states=None, dt_softplus=True,
-                dt_limit=(0.0, math.inf), nthreads=None):
+                dt_limit=(0.0, math.inf), nthreads=None, z=None):
     """Sequential fp64 recurrence over packed varlen sequences.
 
     x [T,H,P], dt [T,H], B and C [T,G,N], A/D/dt_bias [H], cu_seqlens [S+1],
     cu_chunk_seqlens [K+1] (optional), initial_states [S,H,P,N] with the
     boolean has_initial_states [S].  Returns ``(y [T,H,P], chunk_states
     [K,H,P,N] or None, final_states [S,H,P,N])``, all fp64.  chunk_states[k]
-    is the state right after the last token of chunk k.
+    is the state right after the last token of chunk k.  With a gate z
+    [T,H,P], y is y * silu(z) (the state does not see z).
     """
     x = _f64(x); dt = _f64(dt); A = _f64(A); B = _f64(B); C = _f64(C)
     D = _f64(D); dt_bias = _f64(dt_bias)
@@ -146,6 +161,10 @@ def ssd_prefill(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens=None, D=None, dt_bi
         int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError("oracle_ssd_prefill rejected its arguments (code %d)" % rc)
+    if z is not None:
+        zz = _f64(z)
+        assert zz.shape == (T, H, P)
+        y = y * silu(zz)
     return y, cs, fs
 
 
@@ -217,7 +236,7 @@ def prefill_slots(meta, num_computed_tokens, chunk_size, null_block_id, block_ta
 
 def prefill_with_cache(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, init_slot, chunk_slot,
                        null_block_id, cache, D=None, dt_bias=None, dt_softplus=True,
-                       dt_limit=(0.0, math.inf), nthreads=None):
+                       dt_limit=(0.0, math.inf), nthreads=None, z=None):
     """Prefill against a state cache ``cache`` [slots,H,P,N] (numpy, any float).
 
     Every initial state is read before any state is written; chunk end
@@ -234,7 +253,7 @@ def prefill_with_cache(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, init_slot, 
             has[r] = True
     y, cs, _ = ssd_prefill(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, D=D, dt_bias=dt_bias,
                            initial_states=init, has_initial_states=has,
-                           dt_softplus=dt_softplus, dt_limit=dt_limit, nthreads=nthreads)
+                           dt_softplus=dt_softplus, dt_limit=dt_limit, nthreads=nthreads, z=z)
     new_cache = np.array(cache, dtype=np.float64, copy=True)
     for k in range(len(chunk_slot)):
         if int(chunk_slot[k]) != null_block_id:
@@ -243,7 +262,7 @@ def prefill_with_cache(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, init_slot, 
 
 
 def ssm_decode(x, dt, A, B, C, read_states, live, D=None, dt_bias=None, dt_softplus=True,
-               dt_limit=(0.0, math.inf), nthreads=None):
+               dt_limit=(0.0, math.inf), nthreads=None, z=None):
     """Decode update for R requests of ``tpr`` tokens each.
 
     x [R*tpr,H,P], dt [R*tpr,H], B/C [R*tpr,G,N], read_states [R,H,P,N] (the
@@ -263,7 +282,7 @@ def ssm_decode(x, dt, A, B, C, read_states, live, D=None, dt_bias=None, dt_softp
     cc = np.arange(0, T + 1, dtype=np.int32)
     y, cs, _ = ssd_prefill(x, dt, A, B, C, cu, cc, D=D, dt_bias=dt_bias,
                            initial_states=read_states, has_initial_states=np.ones(R, bool),
-                           dt_softplus=dt_softplus, dt_limit=dt_limit, nthreads=nthreads)
+                           dt_softplus=dt_softplus, dt_limit=dt_limit, nthreads=nthreads, z=z)
     states = cs.reshape(R, tpr, H, P, N)
     dead = ~np.asarray(live, dtype=bool)
     y = y.reshape(R, tpr, H, P)
@@ -285,7 +304,7 @@ def decode_read_slots(state_indices, num_accepted_tokens, null_block_id):
 
 def decode_with_cache(x, dt, A, B, C, state_indices, num_accepted_tokens, null_block_id, cache,
                       D=None, dt_bias=None, dt_softplus=True, dt_limit=(0.0, math.inf),
-                      nthreads=None):
+                      nthreads=None, z=None):
     """Decode against a cache: rows whose read slot is null are skipped; the
     state after token k goes to column k unless that slot is null.  Reads
     happen before writes.  Returns ``(y, live, new_cache)``."""
@@ -301,7 +320,7 @@ def decode_with_cache(x, dt, A, B, C, state_indices, num_accepted_tokens, null_b
         if live[r]:
             read[r] = cache[int(rd[r])]
     y, states = ssm_decode(x, dt, A, B, C, read, live, D=D, dt_bias=dt_bias,
-                           dt_softplus=dt_softplus, dt_limit=dt_limit, nthreads=nthreads)
+                           dt_softplus=dt_softplus, dt_limit=dt_limit, nthreads=nthreads, z=z)
     new_cache = np.array(cache, dtype=np.float64, copy=True)
     for r in range(R):
         if not live[r]:

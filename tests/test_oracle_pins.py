@@ -329,3 +329,49 @@ def test_decode_routing_spec_columns_and_null_rows(oracle_lib, null):
     for s in range(12):
         if s not in written:
             assert np.array_equal(new_cache[s], cache[s])
+
+
+def test_silu_gate_values(oracle_lib):
+    """Pin 12a: the oracle's silu equals z * expit(z)
+    from scipy and the closed forms silu(0) = 0, silu(ln 3) = (3/4) ln 3
+    (sigmoid(ln 3) = 3/4), silu(-ln 3) = -(1/4) ln 3, and silu(z) -> z, -> 0 at
+    the two ends."""
+    special = pytest.importorskip("scipy.special")
+    z = np.linspace(-60.0, 60.0, 2001)
+    assert np.allclose(oracle_lib.silu(z), z * special.expit(z), rtol=1e-14, atol=1e-300)
+    l3 = math.log(3.0)
+    assert oracle_lib.silu(np.array([0.0]))[0] == 0.0
+    assert abs(oracle_lib.silu(np.array([l3]))[0] - 0.75 * l3) < 1e-15
+    assert abs(oracle_lib.silu(np.array([-l3]))[0] + 0.25 * l3) < 1e-15
+    assert oracle_lib.silu(np.array([40.0]))[0] == pytest.approx(40.0, rel=1e-15)
+    assert abs(oracle_lib.silu(np.array([-40.0]))[0]) < 1e-15
+
+
+def test_gate_scales_output_only(oracle_lib):
+    """Pin 12b: a gate z multiplies y elementwise by silu(z) and leaves every
+    state untouched; hand-expanded on the scalar filter of pin 6 (two
+    tokens), and on a random varlen batch against the ungated run with an
+    independently computed z * expit(z)."""
+    special = pytest.importorskip("scipy.special")
+    A, D, bias, h0 = -0.5, 0.25, 0.3, 0.9
+    dts, xs, Bs, Cs, zs = [0.2, -1.0], [1.5, -2.0], [0.3, 1.2], [2.0, -0.5], [0.7, -1.3]
+    d = [math.log(1.0 + math.exp(v + bias)) for v in dts]
+    h1 = math.exp(d[0] * A) * h0 + d[0] * xs[0] * Bs[0]
+    h2 = math.exp(d[1] * A) * h1 + d[1] * xs[1] * Bs[1]
+    sig = [1.0 / (1.0 + math.exp(-v)) for v in zs]
+    yexp = [(Cs[0] * h1 + D * xs[0]) * zs[0] * sig[0], (Cs[1] * h2 + D * xs[1]) * zs[1] * sig[1]]
+    sh = lambda v: np.array(v, np.float64).reshape(2, 1, 1)
+    y, _, fs = oracle_lib.ssd_prefill(sh(xs), np.array(dts).reshape(2, 1), np.array([A]), sh(Bs), sh(Cs),
+                                      [0, 2], D=np.array([D]), dt_bias=np.array([bias]),
+                                      initial_states=np.array([[[[h0]]]]), z=sh(zs))
+    assert np.allclose(y.ravel(), yexp, rtol=1e-14, atol=0)
+    assert abs(fs.ravel()[0] - h2) < 1e-14
+    rng = np.random.default_rng(7)
+    T, H, P, N, G = 40, 4, 3, 5, 2
+    x, dt, A, B, C, D, dt_bias = _rand_case(rng, T, H, P, N, G)
+    z = 3.0 * rng.standard_normal((T, H, P))
+    cu, cc = [0, 17, 17, 40], [0, 8, 17, 30, 40]
+    y0, cs0, fs0 = oracle_lib.ssd_prefill(x, dt, A, B, C, cu, cc, D=D, dt_bias=dt_bias)
+    y1, cs1, fs1 = oracle_lib.ssd_prefill(x, dt, A, B, C, cu, cc, D=D, dt_bias=dt_bias, z=z)
+    assert np.array_equal(cs0, cs1) and np.array_equal(fs0, fs1)
+    assert np.allclose(y1, y0 * z * special.expit(z), rtol=1e-13, atol=1e-300)
