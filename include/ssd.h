@@ -59,7 +59,7 @@ typedef struct CUstream_st *ssd_stream_t;
 typedef enum {
     SSD_OK = 0,
     SSD_ERR_INVALID_ARG = 1, /* a size, pointer, alignment or index argument is invalid */
-    SSD_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. z != NULL) */
+    SSD_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. a shape no kernel takes) */
     SSD_ERR_WORKSPACE = 3,   /* workspace (or max_chunks) too small */
     SSD_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
 } ssd_status_t;
@@ -178,7 +178,9 @@ typedef struct ssd_prefill_args {
     const void *dt;      /* [T, H]     dtype */
     const void *B;       /* [T, G, N]  dtype, 16-byte aligned */
     const void *C;       /* [T, G, N]  dtype, 16-byte aligned */
-    const void *z;       /* gate; must be NULL (SSD_ERR_UNSUPPORTED otherwise) */
+    const void *z;       /* [T, H, P] dtype, 16-byte aligned, or NULL: output gate, y is replaced by
+                            y * silu(z) = y * z / (1 + exp(-z)) (the z argument of the chunk-scan
+                            call in "mamba_mixer2.py 변경 사항 (핵심)"; NULL there) */
     const float *A;      /* [H] (negative for a decaying state) */
     const float *D;      /* [H] or NULL (no skip term) */
     const float *dt_bias; /* [H] or NULL (zero) */
@@ -274,7 +276,7 @@ typedef struct ssm_decode_args {
     const void *dt; /* [R * tokens_per_req, H] */
     const void *B;  /* [R * tokens_per_req, G, N] */
     const void *C;  /* [R * tokens_per_req, G, N] */
-    const void *z;  /* must be NULL */
+    const void *z;  /* [R * tokens_per_req, H, P] or NULL: output gate, y * silu(z) as in prefill */
     const float *A, *D, *dt_bias;      /* [H]; D and dt_bias may be NULL */
     float *state_cache;                /* [num_slots, H, P, N] fp32, updated in place */
     const int32_t *state_indices;      /* [R, state_indices_cols] */

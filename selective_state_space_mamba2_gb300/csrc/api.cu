@@ -24,14 +24,13 @@ ssd_status_t check_prefill(const ssd_prefill_args *a) {
     if (a->total_tokens < 0 || a->num_seqs < 0 || a->num_chunks < 0) return SSD_ERR_INVALID_ARG;
     if (!dims_ok(a->nheads, a->headdim, a->dstate, a->ngroups)) return SSD_ERR_INVALID_ARG;
     if (!dtype_ok(a->dtype) || !limits_ok(a->dt_min, a->dt_max)) return SSD_ERR_INVALID_ARG;
-    if (a->z) return SSD_ERR_UNSUPPORTED;
     if (a->num_chunks > 0 && (a->total_tokens == 0 || a->num_seqs == 0)) return SSD_ERR_INVALID_ARG;
     if (a->total_tokens > 0 && a->num_chunks == 0) return SSD_ERR_INVALID_ARG;
     if (a->total_tokens == 0) return SSD_OK;
     if (!a->x || !a->dt || !a->B || !a->C || !a->A || !a->y || !a->cu_seqlens ||
         !a->cu_chunk_seqlens || !a->last_chunk_indices)
         return SSD_ERR_INVALID_ARG;
-    if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->y))
+    if (!aligned16(a->x) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->y) || (a->z && !aligned16(a->z)))
         return SSD_ERR_INVALID_ARG;
     if ((a->init_slot || a->chunk_slot) && (!a->state_cache || a->num_slots <= 0 || !aligned16(a->state_cache)))
         return SSD_ERR_INVALID_ARG;
@@ -93,7 +92,6 @@ extern "C" ssd_status_t ssm_decode_update(const ssm_decode_args *a, ssd_stream_t
         return SSD_ERR_INVALID_ARG;
     if (!dims_ok(a->nheads, a->headdim, a->dstate, a->ngroups)) return SSD_ERR_INVALID_ARG;
     if (!dtype_ok(a->dtype) || !limits_ok(a->dt_min, a->dt_max)) return SSD_ERR_INVALID_ARG;
-    if (a->z) return SSD_ERR_UNSUPPORTED;
     if (a->batch == 0) return SSD_OK;
     if (!a->x || !a->dt || !a->B || !a->C || !a->A || !a->y || !a->state_cache || !a->state_indices ||
         a->num_slots <= 0)

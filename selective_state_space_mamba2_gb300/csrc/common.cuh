@@ -20,6 +20,12 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 template <typename T> __device__ __forceinline__ float ldg_f32(const T *p) { return to_f32(__ldg(p)); }
 
+// Output gate: y * silu(z) = y * z * sigmoid(z) (the optional z argument of the
+// chunk-scan call on "[vllm] vLLM Mamba2 SSD 커널 웜업", section
+// "mamba_mixer2.py 변경 사항 (핵심)").  For z below about -88, __expf(-z) is
+// +inf and the quotient is the right limit, 0.
+__device__ __forceinline__ float silu_gate(float y, float z) { return y * (z / (1.f + __expf(-z))); }
+
 // ---- the per-token step size ----------------------------------------------
 // delta = clamp(softplus(dt + dt_bias), dt_min, dt_max).  softplus(v) is taken
 // as v itself above 20, where log1p(exp(v)) - v < 2.1e-9 * v (below fp32

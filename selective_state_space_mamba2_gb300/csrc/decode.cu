@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kThreads)
     const Tin *dtp = static_cast<const Tin *>(a.dt);
     const Tin *Bp = static_cast<const Tin *>(a.B);
     const Tin *Cp = static_cast<const Tin *>(a.C);
+    const Tin *z = static_cast<const Tin *>(a.z);  // output gate or NULL
     Tin *y = static_cast<Tin *>(a.y);
 
     for (int k = 0; k < tpr; ++k) {
@@ -104,8 +105,11 @@ __global__ void __launch_bounds__(kThreads)
             if (e < nvec && (threadIdx.x & (seg - 1)) == 0) atomicAdd(&sy[p], part);
         }
         __syncthreads();
-        for (int j = tid; j < P; j += kThreads)
-            y[(row * H + h) * P + j] = from_f32<Tin>(sy[j] + Dh * sx[j]);
+        for (int j = tid; j < P; j += kThreads) {
+            const size_t o = (row * H + h) * P + j;
+            const float v = sy[j] + Dh * sx[j];
+            y[o] = from_f32<Tin>(z ? silu_gate(v, ldg_f32(z + o)) : v);
+        }
         const int32_t ws = row_slots[k];
         if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr)) {
             float4 *dst = reinterpret_cast<float4 *>(a.state_cache + (size_t)ws * H * PN + head_off);

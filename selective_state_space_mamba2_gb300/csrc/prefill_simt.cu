@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_
     const Tin *x = static_cast<const Tin *>(a.x);
     const Tin *B = static_cast<const Tin *>(a.B);
     const Tin *C = static_cast<const Tin *>(a.C);
+    const Tin *z = static_cast<const Tin *>(a.z);  // output gate or NULL
     Tin *y = static_cast<Tin *>(a.y);
     const size_t hrow = (size_t)h * a.total_tokens;
     const float Dh = a.D ? a.D[h] : 0.f;
@@ -293,7 +294,8 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(const ssd_prefill_
                 const int t = ta + rr;
                 if (rr < kScanRows && t < tb) {
                     const size_t o = ((size_t)t * H + h) * P + my_p;
-                    y[o] = from_f32<Tin>(acc[i] + Dh * ldg_f32(x + o));
+                    const float v = acc[i] + Dh * ldg_f32(x + o);
+                    y[o] = from_f32<Tin>(z ? silu_gate(v, ldg_f32(z + o)) : v);
                 }
             }
         }

@@ -43,7 +43,6 @@ cudaError_t scratch_on_current_device(void **addr) {
 extern "C" ssd_status_t ssd_prefill_varlen_noalloc(const ssd_prefill_args *a, ssd_stream_t stream) {
     // the same host checks as ssd_prefill_varlen, through its public size query
     if (!a) return SSD_ERR_INVALID_ARG;
-    if (a->z) return SSD_ERR_UNSUPPORTED;
     if (ssd_prefill_kernel_count(a) < 0) return SSD_ERR_INVALID_ARG;
     if (a->total_tokens == 0) return SSD_OK;
     if (!ssd::simt_prefill_supported(*a)) return SSD_ERR_UNSUPPORTED;

@@ -56,6 +56,7 @@ struct TcParams {
     const int32_t *cu_seqlens, *cu_chunk, *last_chunk;
     const int32_t *init_slot, *chunk_slot;
     float *cache;
+    const __nv_bfloat16 *z;  // output gate [T, H, P] or NULL
     __nv_bfloat16 *y;
     uint32_t *err;
     const int32_t *seq_order;
@@ -98,7 +99,9 @@ enum {
     FULL_X0, FULL_X1, FULL_X2, EMPTY_X0, EMPTY_X1, EMPTY_X2,  // x ring: freed after y (EMPTY: 4 arrivals)
     S_RDY0, S_RDY1,                                    // S of the block, per S buffer
     OPS_W,     // producer wg: w x and fp16 x of the block are in smem          (4 arrivals)
-    PRDY,      // producer wg: P of the block is in TMEM                        (4)
+    PRDY0, PRDY1,  // producer wg: P of the block is in TMEM, per S buffer          (4)
+                   // (one barrier per buffer: M1 of the next block goes out before M2 of this
+                   // one, so the P pass can run two blocks ahead of the MMA warp's wait)
     OPS_H,     // consumer wg: fp16 state entering the block is in smem         (4)
     DS_FREE,   // consumer wg: read dS of the previous block                    (4)
     Y1_FREE,   // consumer wg: read Y1 of the previous block                    (4)
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int b = 0; b < NBAR; ++b) {
-            const bool four = b == OPS_W || b == PRDY || b == OPS_H || b == DS_FREE || b == Y1_FREE ||
+            const bool four = b == OPS_W || b == PRDY0 || b == PRDY1 || b == OPS_H || b == DS_FREE || b == Y1_FREE ||
                               (b >= EMPTY_X0 && b <= EMPTY_X2);
             mbar_init(&bar[b], four ? 4 : 1);
         }
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         issue_m1(i + 1);
                         ++m1_issued;
                     }
-                    if (mbar_try_wait(&bar[PRDY], i & 1) && mbar_try_wait(&bar[Y1_FREE], i & 1)) break;
+                    if (mbar_try_wait(&bar[PRDY0 + s], (i >> 1) & 1) && mbar_try_wait(&bar[Y1_FREE], i & 1)) break;
                     if (clock64() - t0 > 2000000000ll) {
                         ok = false;
                         break;
@@ -523,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[PRDY]);
+            if (lane == 0) mbar_arrive(&bar[PRDY0 + s]);
         }
     } else {
         // ------------------------------------ consumer warpgroup (E) -------
@@ -610,14 +613,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    uint4 v;
-                    uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+                    float yv[8];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int e = 8 * cc + 2 * u;
-                        vv[u] = pack_bf16(fmaf(e_row, __uint_as_float(y2[e]), __uint_as_float(y1[e])),
-                                          fmaf(e_row, __uint_as_float(y2[e + 1]), __uint_as_float(y1[e + 1])));
+                    for (int u = 0; u < 8; ++u)
+                        yv[u] = fmaf(e_row, __uint_as_float(y2[8 * cc + u]), __uint_as_float(y1[8 * cc + u]));
+                    if (p.z) {  // output gate y * silu(z); warp-uniform, so the warp stays converged
+                        // for the tcgen05 loads that follow (rows past the block end read a clamped
+                        // token and are never stored)
+                        const size_t zrow = (size_t)min(tb + t, p.T - 1);
+                        const uint4 zz =
+                            *reinterpret_cast<const uint4 *>(p.z + (zrow * p.H + h) * kP + 32 * half + 8 * cc);
+                        const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            yv[2 * u] = silu_gate(yv[2 * u], __uint_as_float(zw[u] << 16));
+                            yv[2 * u + 1] = silu_gate(yv[2 * u + 1], __uint_as_float(zw[u] & 0xFFFF0000u));
+                        }
                     }
+                    const uint4 v = make_uint4(pack_bf16(yv[0], yv[1]), pack_bf16(yv[2], yv[3]),
+                                               pack_bf16(yv[4], yv[5]), pack_bf16(yv[6], yv[7]));
                     *reinterpret_cast<uint4 *>(sY + sw128_offset(t, 4 * half + cc)) = v;
                 }
             }
@@ -707,6 +721,7 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
     p.init_slot = a.init_slot;
     p.chunk_slot = a.chunk_slot;
     p.cache = a.state_cache;
+    p.z = static_cast<const __nv_bfloat16 *>(a.z);
     p.y = static_cast<__nv_bfloat16 *>(a.y);
     p.err = a.err_word;
     p.seq_order = a.seq_order;

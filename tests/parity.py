@@ -116,7 +116,7 @@ def _head_subset(case, heads):
 
 
 def oracle_prefill(case, meta, cache_before, heads=None, D="case", dt_bias="case",
-                   dt_limit=(0.0, math.inf), dt_softplus=True):
+                   dt_limit=(0.0, math.inf), dt_softplus=True, z=None):
     """fp64 oracle on all heads, or on ``heads`` only (each with its group's
     B/C, as an independent one-head-per-group problem).  Returns
     (y [T,h,P], chunk_states [K,h,P,N])."""
@@ -131,6 +131,7 @@ def oracle_prefill(case, meta, cache_before, heads=None, D="case", dt_bias="case
         x, dt = x[:, hs], dt[:, hs]
         B, C = B[:, gs], C[:, gs]
         A = A[hs]
+        z = None if z is None else z[:, hs]
         Dv = None if Dv is None else Dv[hs]
         bv = None if bv is None else bv[hs]
     S = len(meta["init_slot"])
@@ -150,7 +151,8 @@ def oracle_prefill(case, meta, cache_before, heads=None, D="case", dt_bias="case
     y, cs, _ = oracle.ssd_prefill(x.cpu(), dt.cpu(), A.cpu(), B.cpu(), C.cpu(), case["cu_seqlens"],
                                   meta["cu_chunk_seqlens"], D=None if Dv is None else Dv.cpu(),
                                   dt_bias=None if bv is None else bv.cpu(), initial_states=init,
-                                  has_initial_states=has, dt_softplus=dt_softplus, dt_limit=dt_limit)
+                                  has_initial_states=has, dt_softplus=dt_softplus, dt_limit=dt_limit,
+                                  z=None if z is None else z.cpu())
     return y, cs
 
 
@@ -193,7 +195,7 @@ def run_decode(case, err=None, **kw):
     return y
 
 
-def check_decode(case, y_gpu, cache_before, cache_after, requests=None, check_untouched=True):
+def check_decode(case, y_gpu, cache_before, cache_after, requests=None, check_untouched=True, z=None):
     """Oracle decode for ``requests`` (all rows if None): y, every written
     state, padded rows untouched, and every slot no live request writes
     bit-identical."""
@@ -215,7 +217,7 @@ def check_decode(case, y_gpu, cache_before, cache_after, requests=None, check_un
     yo, st = oracle.ssm_decode(case["x"][rows].cpu(), case["dt"][rows].cpu(), case["A"].cpu(),
                                case["B"][rows].cpu(), case["C"][rows].cpu(), read,
                                [rd[r] != null for r in req], D=case["D"].cpu(),
-                               dt_bias=case["dt_bias"].cpu())
+                               dt_bias=case["dt_bias"].cpu(), z=None if z is None else z[rows].cpu())
     yg = y_gpu[rows].double().cpu().numpy()
     liverows = np.array([rd[r] != null for r in req for _ in range(tpr)])
     e_y = y_err(yg[liverows], yo[liverows], case["x"].dtype)

@@ -106,7 +106,7 @@ def _prefill_args(**over):
     (dict(ngroups=3), B.SSD_ERR_INVALID_ARG),
     (dict(headdim=257), B.SSD_ERR_INVALID_ARG),
     (dict(dtype=7), B.SSD_ERR_INVALID_ARG),
-    (dict(z=0x20000), B.SSD_ERR_UNSUPPORTED),
+    (dict(z=0x20008), B.SSD_ERR_INVALID_ARG),  # the gate must be 16-byte aligned too
     (dict(x=0x10008), B.SSD_ERR_INVALID_ARG),
     (dict(x=None), B.SSD_ERR_INVALID_ARG),
     (dict(dt_min=1.0, dt_max=0.5), B.SSD_ERR_INVALID_ARG),
@@ -148,7 +148,6 @@ def _decode_args(**over):
     (dict(tokens_per_req=0), B.SSD_ERR_INVALID_ARG),
     (dict(tokens_per_req=2), B.SSD_ERR_INVALID_ARG),  # fewer columns than tokens
     (dict(ngroups=3), B.SSD_ERR_INVALID_ARG),
-    (dict(z=0x20000), B.SSD_ERR_UNSUPPORTED),
     (dict(state_cache=0x10004), B.SSD_ERR_INVALID_ARG),
     (dict(dstate=6), B.SSD_ERR_INVALID_ARG),
     (dict(dstate=12), B.SSD_ERR_UNSUPPORTED),

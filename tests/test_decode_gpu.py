@@ -36,6 +36,23 @@ def test_spec_decode_small(dtype, null):
     assert nlive == 5 and e_y <= tol and e_s <= tol and same, (e_y, e_s, same)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_spec_decode_output_gate(dtype):
+    """The output gate z on the decode path: y * silu(z) for every token of
+    the live requests; states and padded rows as without a gate."""
+    case = W.decode_case(22, live=5, padded=8, tokens_per_req=3, H=4, P=64, N=128, G=2, num_slots=40,
+                         dtype=dtype, device=DEV, null_block_id=0)
+    g = torch.Generator(device=DEV).manual_seed(98)
+    z = (3.0 * torch.randn(case["x"].shape, generator=g, device=DEV)).to(dtype)
+    before = case["cache"].clone()
+    err = _err()
+    y = PT.run_decode(case, err=err, z=z)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    e_y, e_s, same, tol, nlive = PT.check_decode(case, y, before, case["cache"], z=z)
+    assert nlive == 5 and e_y <= tol and e_s <= tol and same, (e_y, e_s, same)
+
+
 @pytest.mark.parametrize("N,P", [(16, 8), (64, 32), (256, 64)])
 def test_decode_other_state_sizes(N, P):
     case = W.decode_case(22, live=3, padded=4, tokens_per_req=2, H=2, P=P, N=N, G=1, num_slots=12,

@@ -28,7 +28,7 @@ def _run_and_check(case, heads=None, **kw):
     err = _err()
     y, meta = PT.run_prefill(case, err=err, **kw)
     torch.cuda.synchronize()
-    okw = {k: kw[k] for k in ("D", "dt_bias", "dt_limit", "dt_softplus") if k in kw}
+    okw = {k: kw[k] for k in ("D", "dt_bias", "dt_limit", "dt_softplus", "z") if k in kw}
     e_y, e_s, same, tol = PT.check_prefill(case, y, meta, before, case["cache"], heads=heads, **okw)
     assert int(err.item()) == 0
     assert e_y <= tol, ("y", e_y, tol)
@@ -159,3 +159,18 @@ def test_inconsistent_metadata_is_reported():
     PT.run_prefill(case, meta=meta, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & ssd.DEVERR_METADATA
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_output_gate(dtype):
+    """The output gate z: y * silu(z) on the ragged varlen batch (the
+    tensor-core kernel for bf16, the CUDA-core kernels for fp32), with z wide
+    enough (3 N(0,1)) to reach both tails of silu."""
+    new = [300, 1, 0, 129, 64, 517]
+    nc = [10, 64, 0, 63, 0, 200]
+    has = [True, True, False, False, False, True]
+    case = W.prefill_case(12, new, nc, 4, 64, 128, 2, 64, dtype=dtype, device=DEV, has_init=has,
+                          null_block_id=0, num_slots=200)
+    g = torch.Generator(device=DEV).manual_seed(99)
+    z = (3.0 * torch.randn(case["x"].shape, generator=g, device=DEV)).to(dtype)
+    _run_and_check(case, z=z)
