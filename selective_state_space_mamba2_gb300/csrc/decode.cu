@@ -20,8 +20,11 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <typename Tin, int VPT>
-__global__ void __launch_bounds__(kThreads)
+// At least 4 resident CTAs per SM (at most 64 registers) while the state takes up to 32
+// floats per thread: the kernel is HBM-bound, and occupancy is what keeps enough state loads
+// in flight.  The 64-float case keeps its registers (2 CTAs per SM).
+template <typename Tin, int VPT, bool kGate>
+__global__ void __launch_bounds__(kThreads, VPT >= 16 ? 2 : 4)
     ssm_decode_kernel(const ssm_decode_args a) {
     const int r = blockIdx.x;
     const int h = blockIdx.y;
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kThreads)
         for (int j = tid; j < P; j += kThreads) {
             const size_t o = (row * H + h) * P + j;
             const float v = sy[j] + Dh * sx[j];
-            y[o] = from_f32<Tin>(z ? silu_gate(v, ldg_f32(z + o)) : v);
+            y[o] = from_f32<Tin>(kGate ? silu_gate(v, ldg_f32(z + o)) : v);
         }
         const int32_t ws = row_slots[k];
         if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr)) {
@@ -127,11 +130,19 @@ cudaError_t launch_typed(const ssm_decode_args &a, cudaStream_t st) {
     const int nvec = a.headdim * a.dstate / 4;
     const int vpt = (nvec + kThreads - 1) / kThreads;
     dim3 grid(a.batch, a.nheads);
-    if (vpt <= 1) ssm_decode_kernel<Tin, 1><<<grid, kThreads, 0, st>>>(a);
-    else if (vpt <= 2) ssm_decode_kernel<Tin, 2><<<grid, kThreads, 0, st>>>(a);
-    else if (vpt <= 4) ssm_decode_kernel<Tin, 4><<<grid, kThreads, 0, st>>>(a);
-    else if (vpt <= 8) ssm_decode_kernel<Tin, 8><<<grid, kThreads, 0, st>>>(a);
-    else ssm_decode_kernel<Tin, 16><<<grid, kThreads, 0, st>>>(a);
+    if (a.z) {  // gated instances: y * silu(z)
+        if (vpt <= 1) ssm_decode_kernel<Tin, 1, true><<<grid, kThreads, 0, st>>>(a);
+        else if (vpt <= 2) ssm_decode_kernel<Tin, 2, true><<<grid, kThreads, 0, st>>>(a);
+        else if (vpt <= 4) ssm_decode_kernel<Tin, 4, true><<<grid, kThreads, 0, st>>>(a);
+        else if (vpt <= 8) ssm_decode_kernel<Tin, 8, true><<<grid, kThreads, 0, st>>>(a);
+        else ssm_decode_kernel<Tin, 16, true><<<grid, kThreads, 0, st>>>(a);
+    } else {
+        if (vpt <= 1) ssm_decode_kernel<Tin, 1, false><<<grid, kThreads, 0, st>>>(a);
+        else if (vpt <= 2) ssm_decode_kernel<Tin, 2, false><<<grid, kThreads, 0, st>>>(a);
+        else if (vpt <= 4) ssm_decode_kernel<Tin, 4, false><<<grid, kThreads, 0, st>>>(a);
+        else if (vpt <= 8) ssm_decode_kernel<Tin, 8, false><<<grid, kThreads, 0, st>>>(a);
+        else ssm_decode_kernel<Tin, 16, false><<<grid, kThreads, 0, st>>>(a);
+    }
     return cudaGetLastError();
 }
 

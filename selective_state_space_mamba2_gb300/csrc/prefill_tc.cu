@@ -188,6 +188,9 @@ __device__ __forceinline__ void store_state_row(uint8_t *sH, int n, const float 
     }
 }
 
+// kGate: y is multiplied by silu(z) (a separate instance, so the ungated kernel keeps its
+// registers for the rest of the epilogue)
+template <bool kGate>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -617,9 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
                         yv[u] = fmaf(e_row, __uint_as_float(y2[8 * cc + u]), __uint_as_float(y1[8 * cc + u]));
-                    if (p.z) {  // output gate y * silu(z); warp-uniform, so the warp stays converged
-                        // for the tcgen05 loads that follow (rows past the block end read a clamped
-                        // token and are never stored)
+                    if (kGate) {  // output gate y * silu(z); rows past the block end read a clamped
+                                  // token (no lane-dependent branch between tcgen05 loads) and are
+                                  // never stored
                         const size_t zrow = (size_t)min(tb + t, p.T - 1);
                         const uint4 zz =
                             *reinterpret_cast<const uint4 *>(p.z + (zrow * p.H + h) * kP + 32 * half + 8 * cc);
@@ -725,12 +728,12 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
     p.y = static_cast<__nv_bfloat16 *>(a.y);
     p.err = a.err_word;
     p.seq_order = a.seq_order;
-    cudaError_t e = cudaFuncSetAttribute(ssd_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    auto kernel = p.z ? ssd_prefill_tc_kernel<true> : ssd_prefill_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long grid = (long long)a.num_seqs * a.nheads;
     if (grid <= 0) return cudaSuccess;
-    ssd_prefill_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(mX, mB, mC, p);
+    kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(mX, mB, mC, p);
     return cudaGetLastError();
 }
 
