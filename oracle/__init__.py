@@ -330,3 +330,81 @@ def decode_with_cache(x, dt, A, B, C, state_indices, num_accepted_tokens, null_b
             if ws != null_block_id:
                 new_cache[ws] = states[r, k]
     return y, live, new_cache
+
+
+def causal_conv1d_varlen(xbc, weight, bias, cu_seqlens, init_states=None, has_init=None,
+                         activation="silu", cu_chunk_seqlens=None):
+    """Depthwise causal conv1d over packed varlen sequences, in fp64.
+
+    The step before the SSM: x, B and C are "hidden_states, B and C after
+    depthwise convolution" ("[vllm] vLLM Mamba2 SSD 커널 웜업", the
+    MambaMixer2 listing), and each layer keeps a conv state per cache block
+    of shape [state_len, conv_dim] ("vLLM v0.20.0 하이브리드 SSM ...", the
+    [num_blocks, 3, 3072] conv tensor of "전체 흐름").  Read as Mamba2's
+    convolution: for channel c and token t of a sequence,
+        out[t, c] = act(bias[c] + sum_k weight[c, k] * in[t - (W-1) + k, c]),
+    where the W-1 inputs before the sequence's first token come from its
+    conv state (zeros without one) and act is silu or the identity.
+
+    xbc [T, D], weight [D, W], bias [D] or None, cu_seqlens [S+1],
+    init_states [S, W-1, D] with has_init [S].  Returns (out [T, D],
+    final_states [S, W-1, D], chunk_states [K, W-1, D] or None): the state
+    after a token is the last W-1 inputs up to and including it.
+    """
+    xbc = _f64(xbc)
+    w = _f64(weight)
+    T, D = xbc.shape
+    W = w.shape[1]
+    b = np.zeros(D) if bias is None else _f64(bias)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    S = len(cu) - 1
+    out = np.empty((T, D))
+    final = np.zeros((S, W - 1, D))
+    cc = None if cu_chunk_seqlens is None else np.asarray(cu_chunk_seqlens, dtype=np.int64)
+    ends = {} if cc is None else {int(cc[k + 1]) - 1: k for k in range(len(cc) - 1)}
+    chunk = None if cc is None else np.zeros((len(cc) - 1, W - 1, D))
+    for r in range(S):
+        a, e = int(cu[r]), int(cu[r + 1])
+        hist = np.zeros((W - 1, D))
+        if init_states is not None and (has_init is None or has_init[r]):
+            hist = _f64(init_states[r]).copy()
+        buf = np.concatenate([hist, xbc[a:e]], axis=0)  # inputs W-1 before a, then the sequence
+        for i in range(e - a):
+            v = b + np.sum(w.T * buf[i:i + W], axis=0)
+            out[a + i] = silu(v) if activation == "silu" else v
+            k = ends.get(a + i)
+            if k is not None:
+                chunk[k] = buf[i + 1:i + W]
+        final[r] = buf[e - a:e - a + W - 1]
+    return out, final, chunk
+
+
+def causal_conv1d_with_cache(xbc, weight, bias, cu_seqlens, cache, init_slot, out_slot, null_block_id,
+                             activation="silu", cu_chunk_seqlens=None, chunk_slot=None):
+    """causal_conv1d_varlen against a conv-state cache [slots, W-1, D]: sequence
+    r starts from slot init_slot[r] (zeros if null), its final state goes to
+    out_slot[r] and each chunk's end state to chunk_slot[k] (unless null);
+    every read happens before any write.  Decode is the same call with one
+    sequence per request.  Returns (out, new_cache)."""
+    S = len(cu_seqlens) - 1
+    W1 = cache.shape[1]
+    D = cache.shape[2]
+    init = np.zeros((S, W1, D))
+    has = np.zeros(S, bool)
+    for r in range(S):
+        s = int(init_slot[r]) if init_slot is not None else null_block_id
+        if s != null_block_id:
+            init[r] = _f64(cache[s])
+            has[r] = True
+    out, final, chunk = causal_conv1d_varlen(xbc, weight, bias, cu_seqlens, init, has, activation,
+                                             cu_chunk_seqlens)
+    new = np.array(cache, dtype=np.float64, copy=True)
+    if chunk_slot is not None:
+        for k in range(len(chunk_slot)):
+            if int(chunk_slot[k]) != null_block_id:
+                new[int(chunk_slot[k])] = chunk[k]
+    if out_slot is not None:
+        for r in range(S):
+            if int(out_slot[r]) != null_block_id:
+                new[int(out_slot[r])] = final[r]
+    return out, new

@@ -375,3 +375,52 @@ def test_gate_scales_output_only(oracle_lib):
     y1, cs1, fs1 = oracle_lib.ssd_prefill(x, dt, A, B, C, cu, cc, D=D, dt_bias=dt_bias, z=z)
     assert np.array_equal(cs0, cs1) and np.array_equal(fs0, fs1)
     assert np.allclose(y1, y0 * z * special.expit(z), rtol=1e-13, atol=1e-300)
+
+
+def test_conv1d_equals_numpy_convolve_per_channel(oracle_lib):
+    """Pin 13a: without history, the oracle's depthwise causal conv of each
+    channel equals numpy's full convolution with the reversed taps, cut to
+    the sequence length, plus the bias; with silu it is that value times
+    scipy's expit of it; with W = 1 it is the elementwise affine map."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(3)
+    L, D, W = 23, 5, 4
+    x = rng.standard_normal((L, D))
+    w = rng.standard_normal((D, W))
+    b = rng.standard_normal(D)
+    out, final, _ = oracle_lib.causal_conv1d_varlen(x, w, b, [0, L], activation="none")
+    ref = np.stack([np.convolve(x[:, c], w[c, ::-1])[:L] + b[c] for c in range(D)], axis=1)
+    assert np.allclose(out, ref, rtol=1e-13, atol=1e-13)
+    assert np.array_equal(final[0], x[L - W + 1:])
+    outs, _, _ = oracle_lib.causal_conv1d_varlen(x, w, b, [0, L], activation="silu")
+    assert np.allclose(outs, ref * special.expit(ref), rtol=1e-13, atol=1e-300)
+    out1, _, _ = oracle_lib.causal_conv1d_varlen(x, w[:, :1], b, [0, L], activation="none")
+    assert np.allclose(out1, x * w[:, 0] + b, rtol=1e-15, atol=1e-15)
+
+
+def test_conv1d_resume_from_state_and_chunk_states(oracle_lib):
+    """Pin 13b: a sequence cut in two, the second part started from the
+    first part's final state, gives the outputs and final state of the whole
+    (also when a part is shorter than W - 1); the state stored at a chunk end
+    is the final state of the prefix ending there; packing sequences
+    changes nothing."""
+    rng = np.random.default_rng(4)
+    D, W = 6, 4
+    for L, cut in [(30, 11), (9, 2), (5, 1)]:
+        x = rng.standard_normal((L, D))
+        w = rng.standard_normal((D, W))
+        b = rng.standard_normal(D)
+        h0 = rng.standard_normal((1, W - 1, D))
+        whole, fw, cs = oracle_lib.causal_conv1d_varlen(x, w, b, [0, L], init_states=h0,
+                                                         cu_chunk_seqlens=[0, cut, L])
+        p1, f1, _ = oracle_lib.causal_conv1d_varlen(x[:cut], w, b, [0, cut], init_states=h0)
+        p2, f2, _ = oracle_lib.causal_conv1d_varlen(x[cut:], w, b, [0, L - cut], init_states=f1)
+        assert np.allclose(whole, np.concatenate([p1, p2]), rtol=1e-14, atol=1e-14)
+        assert np.array_equal(fw, f2) and np.array_equal(cs[0], f1[0]) and np.array_equal(cs[1], fw[0])
+    # packed: two sequences side by side equal two separate calls
+    xa, xb = rng.standard_normal((7, D)), rng.standard_normal((12, D))
+    w = rng.standard_normal((D, W))
+    packed, fp, _ = oracle_lib.causal_conv1d_varlen(np.concatenate([xa, xb]), w, None, [0, 7, 19])
+    oa, fa, _ = oracle_lib.causal_conv1d_varlen(xa, w, None, [0, 7])
+    ob, fb, _ = oracle_lib.causal_conv1d_varlen(xb, w, None, [0, 12])
+    assert np.array_equal(packed, np.concatenate([oa, ob])) and np.array_equal(fp, np.concatenate([fa, fb]))
