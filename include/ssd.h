@@ -298,6 +298,72 @@ typedef struct ssm_decode_args {
  */
 SSD_API ssd_status_t ssm_decode_update(const ssm_decode_args *args, ssd_stream_t stream);
 
+/* ------------------------------------------------------------------------ *
+ * Depthwise causal conv1d before the SSM (device)
+ *
+ * The step that produces x, B and C: "get hidden_states, B and C after
+ * depthwise convolution" in the MambaMixer2 listing of "[vllm] vLLM Mamba2 SSD
+ * 커널 웜업", with a conv state per cache block of shape [state_len, conv_dim]
+ * ("vLLM v0.20.0 하이브리드 SSM 모델을 위한 분산 서빙 추가", "전체 흐름": a
+ * [num_blocks, 3, 3072] conv tensor next to the [num_blocks, 48, 64, 128]
+ * SSM tensor).  For channel c and token t of a sequence,
+ *   out[t, c] = act(bias[c] + sum_{k<W} weight[c, k] * in[t - (W-1) + k, c]),
+ * where the W-1 inputs before the sequence's first token come from its conv
+ * state (zeros without one) and act is silu or the identity.  The conv state
+ * after a token is the last W-1 inputs up to and including it (exact copies,
+ * in the token dtype).
+ * ------------------------------------------------------------------------ */
+typedef struct ssd_conv1d_args {
+    int32_t total_tokens;  /* T */
+    int32_t num_seqs;      /* S (for ssd_conv1d_update: requests R, each tokens_per_req tokens) */
+    int32_t num_chunks;    /* K = cu_chunk_seqlens entries - 1, or 0 when chunk_slot is NULL */
+    int32_t tokens_per_req; /* ssd_conv1d_update only: tokens of each request (>= 1) */
+    int32_t dim_x;         /* channels [0, dim_x) go to x_out */
+    int32_t dim_bc;        /* channels [dim_x, dim_x + dim_bc) to B_out, the next dim_bc to C_out */
+    int32_t width;         /* W, 2..4 taps */
+    int32_t dtype;         /* ssd_dtype_t of xbc, the outputs and conv_state */
+    int32_t activation;    /* 0: identity, 1: silu */
+    int32_t num_slots;     /* rows of conv_state */
+    int32_t null_block_id;
+    /* device pointers */
+    const void *xbc;       /* [T, D] with D = dim_x + 2 dim_bc, 16-byte aligned rows (D % 8 == 0) */
+    const float *weight;   /* [D, W] */
+    const float *bias;     /* [D] or NULL */
+    const int32_t *cu_seqlens;        /* [S+1] (ssd_conv1d_varlen) */
+    const int32_t *cu_chunk_seqlens;  /* [K+1] or NULL (ssd_conv1d_varlen) */
+    const int32_t *last_chunk_indices; /* [S], chunk ranges as for ssd_prefill_varlen, or NULL */
+    const int32_t *init_slot;  /* [S] or NULL: conv state each sequence starts from (null id: zeros);
+                                  for ssd_conv1d_update the request's slot, read and then overwritten */
+    const int32_t *out_slot;   /* [S] or NULL: where the state after each sequence's last token goes */
+    const int32_t *chunk_slot; /* [K] or NULL: where the state after each chunk's last token goes */
+    void *conv_state;      /* [num_slots, W-1, D] dtype, 16-byte aligned */
+    void *x_out;           /* [T, dim_x]  dtype, 16-byte aligned */
+    void *B_out;           /* [T, dim_bc] dtype, 16-byte aligned */
+    void *C_out;           /* [T, dim_bc] dtype, 16-byte aligned */
+    uint32_t *err_word;    /* device word or NULL (SSD_DEVERR_SLOT for an out-of-range slot) */
+} ssd_conv1d_args;
+
+/*
+ * Prefill: packed sequences, cu_seqlens as for ssd_prefill_varlen (the chunk
+ * metadata of ssd_chunk_metadata gives cu_chunk_seqlens, last_chunk_indices
+ * and the slots).  Every conv-state read happens before any conv-state write,
+ * so a sequence's initial slot may also be one of its output slots.  Host
+ * checks: sizes, dim_x and dim_bc multiples of 8, 2 <= W <= 4, pointers and
+ * alignments; SSD_ERR_CUDA if a launch fails.  Two kernels (the convolution,
+ * then the state stores).
+ */
+SSD_API ssd_status_t ssd_conv1d_varlen(const ssd_conv1d_args *args, ssd_stream_t stream);
+
+/*
+ * Decode: R requests of tokens_per_req tokens each (token k of request r is
+ * row r * tokens_per_req + k), the conv state read from init_slot[r] and the
+ * state after the last token written back to the same slot.  A request whose
+ * slot is null_block_id is CUDA-graph padding ("CUDA Graph 지원" of the Mamba
+ * (SSM) page): none of its rows is read or written.  cu_seqlens,
+ * cu_chunk_seqlens, last_chunk_indices, out_slot and chunk_slot are ignored.
+ */
+SSD_API ssd_status_t ssd_conv1d_update(const ssd_conv1d_args *args, ssd_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

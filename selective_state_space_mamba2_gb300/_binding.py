@@ -22,7 +22,7 @@ DEVERR_SLOT, DEVERR_METADATA, DEVERR_COLUMN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1
 
 EXPORTED_SYMBOLS = ("ssd_status_string", "ssd_abi_version", "ssd_max_chunks", "ssd_chunk_metadata",
                     "ssd_prefill_workspace_size", "ssd_prefill_kernel_count", "ssd_prefill_varlen",
-                    "ssd_prefill_varlen_noalloc", "ssm_decode_update")
+                    "ssd_prefill_varlen_noalloc", "ssm_decode_update", "ssd_conv1d_varlen", "ssd_conv1d_update")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -48,6 +48,15 @@ class DecodeArgs(ctypes.Structure):
                 ("x", _vp), ("dt", _vp), ("B", _vp), ("C", _vp), ("z", _vp), ("A", _vp), ("D", _vp),
                 ("dt_bias", _vp), ("state_cache", _vp), ("state_indices", _vp),
                 ("num_accepted_tokens", _vp), ("y", _vp), ("err_word", _vp)]
+
+
+class Conv1dArgs(ctypes.Structure):
+    _fields_ = [("total_tokens", _i32), ("num_seqs", _i32), ("num_chunks", _i32), ("tokens_per_req", _i32),
+                ("dim_x", _i32), ("dim_bc", _i32), ("width", _i32), ("dtype", _i32), ("activation", _i32),
+                ("num_slots", _i32), ("null_block_id", _i32),
+                ("xbc", _vp), ("weight", _vp), ("bias", _vp), ("cu_seqlens", _vp), ("cu_chunk_seqlens", _vp),
+                ("last_chunk_indices", _vp), ("init_slot", _vp), ("out_slot", _vp), ("chunk_slot", _vp),
+                ("conv_state", _vp), ("x_out", _vp), ("B_out", _vp), ("C_out", _vp), ("err_word", _vp)]
 
 
 class SSDError(RuntimeError):
@@ -304,3 +313,85 @@ def ssm_decode_update(x, dt, A, B, C, state_cache, state_indices, num_accepted_t
     if rc != SSD_OK:
         raise SSDError("ssm_decode_update", rc)
     return out
+
+
+def conv1d_args(xbc, weight, dim_x, dim_bc, x_out, B_out, C_out, bias=None, conv_state=None, activation="silu",
+                null_block_id=0, err_word=None):
+    """Arguments shared by the two conv calls (sizes, tensors, activation)."""
+    T, D = xbc.shape
+    if D != dim_x + 2 * dim_bc:
+        raise ValueError("xbc has %d channels, dim_x + 2 dim_bc = %d" % (D, dim_x + 2 * dim_bc))
+    if weight.dtype != torch.float32 or weight.dim() != 2 or weight.shape[0] != D:
+        raise ValueError("weight must be float32 [%d, W]" % D)
+    W = weight.shape[1]
+    for name, t, shp in (("x_out", x_out, (T, dim_x)), ("B_out", B_out, (T, dim_bc)), ("C_out", C_out, (T, dim_bc))):
+        if tuple(t.shape) != shp or t.dtype != xbc.dtype:
+            raise ValueError("%s must be %s of shape %s" % (name, xbc.dtype, shp))
+    if conv_state is not None and (conv_state.dtype != xbc.dtype or tuple(conv_state.shape[1:]) != (W - 1, D)):
+        raise ValueError("conv_state must be %s [slots, %d, %d]" % (xbc.dtype, W - 1, D))
+    a = Conv1dArgs()
+    a.total_tokens, a.dim_x, a.dim_bc, a.width = T, dim_x, dim_bc, W
+    a.dtype = _dtype_code(xbc)
+    a.activation = {"silu": 1, None: 0, "none": 0}[activation]
+    a.num_slots = 0 if conv_state is None else conv_state.shape[0]
+    a.null_block_id = int(null_block_id)
+    a.xbc = _dev(xbc, "xbc")
+    a.weight = _dev(weight, "weight", torch.float32)
+    a.bias = _dev(bias, "bias", torch.float32, required=False)
+    a.conv_state = _dev(conv_state, "conv_state", required=False)
+    a.x_out, a.B_out, a.C_out = _dev(x_out, "x_out"), _dev(B_out, "B_out"), _dev(C_out, "C_out")
+    a.err_word = _dev(err_word, "err_word", required=False)
+    return a
+
+
+def _conv_outputs(xbc, dim_x, dim_bc, x_out, B_out, C_out):
+    T = xbc.shape[0]
+    if x_out is None:
+        x_out = torch.empty((T, dim_x), dtype=xbc.dtype, device=xbc.device)
+    if B_out is None:
+        B_out = torch.empty((T, dim_bc), dtype=xbc.dtype, device=xbc.device)
+    if C_out is None:
+        C_out = torch.empty((T, dim_bc), dtype=xbc.dtype, device=xbc.device)
+    return x_out, B_out, C_out
+
+
+def ssd_conv1d_varlen(xbc, weight, cu_seqlens, dim_x, dim_bc, bias=None, conv_state=None, init_slot=None,
+                      out_slot=None, chunk_slot=None, cu_chunk_seqlens=None, last_chunk_indices=None,
+                      activation="silu", null_block_id=0, x_out=None, B_out=None, C_out=None, err_word=None,
+                      stream=None):
+    """Depthwise causal conv1d over packed sequences; returns (x [T, dim_x], B [T, dim_bc],
+    C [T, dim_bc]).  Device int32 metadata as for ssd_prefill_varlen."""
+    x_out, B_out, C_out = _conv_outputs(xbc, dim_x, dim_bc, x_out, B_out, C_out)
+    a = conv1d_args(xbc, weight, dim_x, dim_bc, x_out, B_out, C_out, bias, conv_state, activation,
+                    null_block_id, err_word)
+    a.num_seqs = cu_seqlens.numel() - 1
+    a.num_chunks = 0 if cu_chunk_seqlens is None else cu_chunk_seqlens.numel() - 1
+    a.cu_seqlens = _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    a.cu_chunk_seqlens = _dev(cu_chunk_seqlens, "cu_chunk_seqlens", torch.int32, required=False)
+    a.last_chunk_indices = _dev(last_chunk_indices, "last_chunk_indices", torch.int32, required=False)
+    a.init_slot = _dev(init_slot, "init_slot", torch.int32, required=False)
+    a.out_slot = _dev(out_slot, "out_slot", torch.int32, required=False)
+    a.chunk_slot = _dev(chunk_slot, "chunk_slot", torch.int32, required=False)
+    rc = lib().ssd_conv1d_varlen(ctypes.byref(a), _stream(stream))
+    if rc != SSD_OK:
+        raise SSDError("ssd_conv1d_varlen", rc)
+    return x_out, B_out, C_out
+
+
+def ssd_conv1d_update(xbc, weight, conv_state, state_indices, dim_x, dim_bc, bias=None, activation="silu",
+                      null_block_id=0, x_out=None, B_out=None, C_out=None, err_word=None, stream=None):
+    """Decode conv step: request r's rows r*tpr .. r*tpr + tpr - 1 continue the conv state in slot
+    state_indices[r], which then holds the state after its last token; null rows are padding."""
+    R = state_indices.numel()
+    T = xbc.shape[0]
+    if R == 0 or T % R:
+        raise ValueError("xbc rows must be a multiple of the requests")
+    x_out, B_out, C_out = _conv_outputs(xbc, dim_x, dim_bc, x_out, B_out, C_out)
+    a = conv1d_args(xbc, weight, dim_x, dim_bc, x_out, B_out, C_out, bias, conv_state, activation,
+                    null_block_id, err_word)
+    a.num_seqs, a.tokens_per_req = R, T // R
+    a.init_slot = _dev(state_indices, "state_indices", torch.int32)
+    rc = lib().ssd_conv1d_update(ctypes.byref(a), _stream(stream))
+    if rc != SSD_OK:
+        raise SSDError("ssd_conv1d_update", rc)
+    return x_out, B_out, C_out

@@ -100,3 +100,45 @@ extern "C" ssd_status_t ssm_decode_update(const ssm_decode_args *a, ssd_stream_t
     if (!ssd::decode_supported(*a)) return SSD_ERR_UNSUPPORTED;
     return from_cuda(ssd::decode_launch(*a, reinterpret_cast<cudaStream_t>(stream)));
 }
+
+namespace {
+
+ssd_status_t check_conv(const ssd_conv1d_args *a, bool decode) {
+    if (!a) return SSD_ERR_INVALID_ARG;
+    if (a->total_tokens < 0 || a->num_seqs < 0 || a->num_chunks < 0) return SSD_ERR_INVALID_ARG;
+    if (a->dim_x < 0 || a->dim_bc < 0 || a->dim_x % 8 != 0 || a->dim_bc % 8 != 0 || a->dim_x + a->dim_bc == 0)
+        return SSD_ERR_INVALID_ARG;
+    if (a->width < 2 || a->width > 4 || (a->activation != 0 && a->activation != 1)) return SSD_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype)) return SSD_ERR_INVALID_ARG;
+    if (decode && (a->tokens_per_req < 1 || (int64_t)a->num_seqs * a->tokens_per_req != a->total_tokens))
+        return SSD_ERR_INVALID_ARG;
+    if (a->total_tokens == 0 && a->num_seqs == 0) return SSD_OK;
+    if (!a->xbc || !a->weight || !aligned16(a->xbc)) return SSD_ERR_INVALID_ARG;
+    if (a->total_tokens > 0 && (!a->x_out || !a->B_out || !a->C_out || !aligned16(a->x_out) ||
+                                !aligned16(a->B_out) || !aligned16(a->C_out)))
+        return SSD_ERR_INVALID_ARG;
+    if (!decode) {
+        if (!a->cu_seqlens) return SSD_ERR_INVALID_ARG;
+        if (a->chunk_slot && (!a->cu_chunk_seqlens || !a->last_chunk_indices || a->num_chunks <= 0))
+            return SSD_ERR_INVALID_ARG;
+    } else if (!a->init_slot) {
+        return SSD_ERR_INVALID_ARG;
+    }
+    const bool uses_state = a->init_slot || (!decode && (a->out_slot || a->chunk_slot));
+    if (uses_state && (!a->conv_state || a->num_slots <= 0 || !aligned16(a->conv_state))) return SSD_ERR_INVALID_ARG;
+    return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" ssd_status_t ssd_conv1d_varlen(const ssd_conv1d_args *a, ssd_stream_t stream) {
+    const ssd_status_t st = check_conv(a, false);
+    if (st != SSD_OK || a->num_seqs == 0) return st;
+    return from_cuda(ssd::conv1d_launch(*a, false, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" ssd_status_t ssd_conv1d_update(const ssd_conv1d_args *a, ssd_stream_t stream) {
+    const ssd_status_t st = check_conv(a, true);
+    if (st != SSD_OK || a->num_seqs == 0) return st;
+    return from_cuda(ssd::conv1d_launch(*a, true, reinterpret_cast<cudaStream_t>(stream)));
+}

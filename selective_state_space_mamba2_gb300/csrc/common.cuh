@@ -25,6 +25,7 @@ template <typename T> __device__ __forceinline__ float ldg_f32(const T *p) { ret
 // "mamba_mixer2.py 변경 사항 (핵심)").  For z below about -88, __expf(-z) is
 // +inf and the quotient is the right limit, 0.
 __device__ __forceinline__ float silu_gate(float y, float z) { return y * (z / (1.f + __expf(-z))); }
+__device__ __forceinline__ float silu(float v) { return v / (1.f + __expf(-v)); }
 
 // ---- the per-token step size ----------------------------------------------
 // delta = clamp(softplus(dt + dt_bias), dt_min, dt_max).  softplus(v) is taken
@@ -75,4 +76,6 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
 
 bool decode_supported(const ssm_decode_args &a);
 cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s);
+
+cudaError_t conv1d_launch(const ssd_conv1d_args &a, bool decode, cudaStream_t s);
 }  // namespace ssd

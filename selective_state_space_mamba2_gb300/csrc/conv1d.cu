@@ -1,0 +1,306 @@
+// Depthwise causal conv1d in front of the SSM, with a conv-state cache.
+//
+// The step that produces x, B and C ("get hidden_states, B and C after
+// depthwise convolution", MambaMixer2 listing of "[vllm] vLLM Mamba2 SSD 커널
+// 웜업"), with the per-block conv state of "vLLM v0.20.0 하이브리드 SSM 모델을
+// 위한 분산 서빙 추가" ("전체 흐름": [num_blocks, 3, 3072]).  For channel c and
+// token t of a sequence,
+//   out[t, c] = act(bias[c] + sum_{k<W} weight[c, k] * in[t - (W-1) + k, c]),
+// with the W-1 inputs before the sequence's first token taken from its conv
+// state (zeros without one).
+//
+// HBM-bound streaming work, no contraction: each thread owns 8 consecutive
+// channels (one 16-byte vector) and a run of kRun consecutive tokens, keeping
+// the W-1 previous inputs in registers as a sliding window, so every input is
+// read once from HBM (plus W-1 rows of overlap per run) and every output written
+// once, coalesced across the warp.  The outputs go straight to three tensors
+// (x, B, C), the layout the SSM calls take.  A second, small kernel then writes
+// the conv states at chunk ends and sequence ends: ordered after the first on
+// the stream, so all state reads precede all state writes.
+#include "common.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kVec = 8;        // channels per thread (16 bytes of bf16)
+constexpr int kRun = 16;       // tokens per thread
+constexpr int kConvThreads = 128;
+
+struct ConvParams {
+    int T, S, K, tpr, D, dim_x, dim_bc, num_slots, null_id, activation;
+    bool decode;               // requests of tpr tokens; null slot = padding (skipped)
+    const float *weight, *bias;
+    const int32_t *cu_seqlens, *cu_chunk, *last_chunk, *init_slot, *out_slot, *chunk_slot;
+    uint32_t *err;
+};
+
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[kVec]) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float (&v)[kVec]) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    // exact copy of an input vector (states hold inputs bit for bit)
+    static __device__ __forceinline__ void copy(__nv_bfloat16 *dst, const __nv_bfloat16 *src) {
+        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+    }
+};
+template <> struct Vec8<float> {
+    static __device__ __forceinline__ void load(const float *p, float (&v)[kVec]) {
+        const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    static __device__ __forceinline__ void store(float *p, const float (&v)[kVec]) {
+        reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    static __device__ __forceinline__ void copy(float *dst, const float *src) {
+        reinterpret_cast<float4 *>(dst)[0] = reinterpret_cast<const float4 *>(src)[0];
+        reinterpret_cast<float4 *>(dst)[1] = reinterpret_cast<const float4 *>(src)[1];
+    }
+};
+
+// sequence holding token t: the last r with cu_seqlens[r] <= t (empty sequences skipped)
+__device__ __forceinline__ int seq_of(const int32_t *cu, int S, int t) {
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    while (lo + 1 < S && cu[lo + 1] <= t) ++lo;  // past empty sequences that start at t
+    return lo;
+}
+
+__device__ __forceinline__ int seq_start(const ConvParams &p, int r) { return p.decode ? r * p.tpr : p.cu_seqlens[r]; }
+__device__ __forceinline__ int seq_end(const ConvParams &p, int r) { return p.decode ? (r + 1) * p.tpr : p.cu_seqlens[r + 1]; }
+
+// conv-state slot sequence r starts from: -1 for zeros, -2 for a skipped (padding) request
+__device__ __forceinline__ int history_slot(const ConvParams &p, int r, bool report_errors) {
+    const int32_t s = p.init_slot ? p.init_slot[r] : p.null_id;
+    if (s == p.null_id) return p.decode ? -2 : -1;
+    if (s < 0 || s >= p.num_slots) {
+        if (report_errors) report(p.err, SSD_DEVERR_SLOT);
+        return p.decode ? -2 : -1;
+    }
+    return s;
+}
+
+// input j steps before token t of sequence r (start s0), for the 8 channels at c0: the
+// token itself when it is inside the sequence, else row (W-1) - (s0 - tau) of the history
+template <typename Tin, int W>
+__device__ __forceinline__ void input_before(const Tin *xbc, const Tin *state, int hslot, int D, int s0, int tau,
+                                             int c0, float (&v)[kVec]) {
+    if (tau >= s0) {
+        Vec8<Tin>::load(xbc + (size_t)tau * D + c0, v);
+    } else if (hslot >= 0) {
+        Vec8<Tin>::load(state + ((size_t)hslot * (W - 1) + (W - 1) - (s0 - tau)) * D + c0, v);
+    } else {
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) v[i] = 0.f;
+    }
+}
+
+template <typename Tin, int W>
+__global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const Tin *__restrict__ xbc, const Tin *state,
+                                                              Tin *x_out, Tin *B_out, Tin *C_out, ConvParams p) {
+    const int vec = blockIdx.x * kConvThreads + threadIdx.x;
+    const int t0 = blockIdx.y * kRun;
+    if (vec * kVec >= p.D || t0 >= p.T) return;
+    const int c0 = vec * kVec;
+    float w[W][kVec], b[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) w[k][i] = p.weight[(size_t)(c0 + i) * W + k];
+        b[i] = p.bias ? p.bias[c0 + i] : 0.f;
+    }
+    // output tensor and column of these channels
+    Tin *out;
+    int ocol, ostride;
+    if (c0 < p.dim_x) {
+        out = x_out, ocol = c0, ostride = p.dim_x;
+    } else if (c0 < p.dim_x + p.dim_bc) {
+        out = B_out, ocol = c0 - p.dim_x, ostride = p.dim_bc;
+    } else {
+        out = C_out, ocol = c0 - p.dim_x - p.dim_bc, ostride = p.dim_bc;
+    }
+    const int t1 = min(t0 + kRun, p.T);
+    int r = p.decode ? t0 / p.tpr : seq_of(p.cu_seqlens, p.S, t0);
+    int s0 = seq_start(p, r), e0 = seq_end(p, r);
+    int hslot = history_slot(p, r, vec == 0);
+    float win[W - 1][kVec];  // win[0] oldest
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j) input_before<Tin, W>(xbc, state, hslot, p.D, s0, t0 - (W - 1) + j, c0, win[j]);
+    for (int t = t0; t < t1; ++t) {
+        if (t >= e0) {  // next sequence (empty ones have no tokens to visit)
+            do {
+                if (r + 1 >= p.S) {  // cu_seqlens does not end at T
+                    if (vec == 0) report(p.err, SSD_DEVERR_METADATA);
+                    return;
+                }
+                ++r;
+                s0 = seq_start(p, r);
+                e0 = seq_end(p, r);
+            } while (e0 <= t);
+            hslot = history_slot(p, r, vec == 0);
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j) input_before<Tin, W>(xbc, state, hslot, p.D, s0, t - (W - 1) + j, c0, win[j]);
+        }
+        float cur[kVec];
+        Vec8<Tin>::load(xbc + (size_t)t * p.D + c0, cur);
+        float o[kVec];
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) {
+            float acc = b[i];
+#pragma unroll
+            for (int k = 0; k < W - 1; ++k) acc = fmaf(w[k][i], win[k][i], acc);
+            acc = fmaf(w[W - 1][i], cur[i], acc);
+            o[i] = p.activation ? silu(acc) : acc;
+        }
+        if (hslot != -2) Vec8<Tin>::store(out + (size_t)t * ostride + ocol, o);
+#pragma unroll
+        for (int j = 0; j + 1 < W - 1; ++j)
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) win[j][i] = win[j + 1][i];
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) win[W - 2][i] = cur[i];
+    }
+}
+
+// Conv states of sequence r: the W-1 inputs ending at each of its chunk ends and at its
+// last token (for a request of the decode call: its own slot).  The history this needs
+// is read into registers before any store, so a slot may be both read and written.
+template <typename Tin, int W>
+__global__ void __launch_bounds__(kConvThreads) conv_state_kernel(const Tin *__restrict__ xbc, Tin *state, ConvParams p) {
+    const int vec = blockIdx.x * kConvThreads + threadIdx.x;
+    const int r = blockIdx.y;
+    if (vec * kVec >= p.D) return;
+    const int c0 = vec * kVec;
+    const int hslot = history_slot(p, r, false);
+    if (hslot == -2) return;  // padding request
+    const int s0 = seq_start(p, r), e0 = seq_end(p, r);
+    if (s0 < 0 || e0 < s0 || e0 > p.T) {
+        if (vec == 0) report(p.err, SSD_DEVERR_METADATA);
+        return;
+    }
+    Tin hist[W - 1][kVec];
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j)
+#pragma unroll
+        for (int i = 0; i < kVec; ++i)
+            hist[j][i] = hslot >= 0 ? state[((size_t)hslot * (W - 1) + j) * p.D + c0 + i] : Tin(0.f);
+    // window ending at token e (inclusive) into slot s
+    auto store_window = [&](int e, int32_t s) {
+        if (s == p.null_id) return;
+        if (s < 0 || s >= p.num_slots) {
+            if (vec == 0) report(p.err, SSD_DEVERR_SLOT);
+            return;
+        }
+#pragma unroll
+        for (int j = 0; j < W - 1; ++j) {
+            const int tau = e - (W - 2) + j;
+            Tin *dst = state + ((size_t)s * (W - 1) + j) * p.D + c0;
+            if (tau >= s0) {
+                Vec8<Tin>::copy(dst, xbc + (size_t)tau * p.D + c0);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kVec; ++i) dst[i] = hist[(W - 1) - (s0 - tau)][i];
+            }
+        }
+    };
+    if (p.decode) {
+        store_window(e0 - 1, p.init_slot[r]);
+        return;
+    }
+    if (p.chunk_slot && p.last_chunk) {
+        const int first = r > 0 ? p.last_chunk[r - 1] + 1 : 0, last = p.last_chunk[r];
+        if (first < 0 || last >= p.K) {
+            if (vec == 0) report(p.err, SSD_DEVERR_METADATA);
+            return;
+        }
+        for (int k = first; k <= last; ++k) {
+            const int e = p.cu_chunk[k + 1] - 1;  // the chunk's last token, inside this sequence
+            if (e < s0 || e >= e0) {
+                if (vec == 0) report(p.err, SSD_DEVERR_METADATA);
+                continue;
+            }
+            store_window(e, p.chunk_slot[k]);
+        }
+    }
+    if (p.out_slot) store_window(e0 - 1, p.out_slot[r]);
+}
+
+template <typename Tin, int W>
+cudaError_t launch_w(const ssd_conv1d_args &a, const ConvParams &p, cudaStream_t st) {
+    const int vecs = p.D / kVec;
+    const dim3 grid1((vecs + kConvThreads - 1) / kConvThreads, (p.T + kRun - 1) / kRun);
+    const Tin *xbc = static_cast<const Tin *>(a.xbc);
+    Tin *state = static_cast<Tin *>(a.conv_state);
+    if (p.T > 0) {
+        conv1d_kernel<Tin, W><<<grid1, kConvThreads, 0, st>>>(xbc, state, static_cast<Tin *>(a.x_out),
+                                                              static_cast<Tin *>(a.B_out),
+                                                              static_cast<Tin *>(a.C_out), p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const bool any_state = p.decode || p.out_slot || (p.chunk_slot && p.last_chunk);
+    if (any_state && p.S > 0) {
+        const dim3 grid2((vecs + kConvThreads - 1) / kConvThreads, p.S);
+        conv_state_kernel<Tin, W><<<grid2, kConvThreads, 0, st>>>(xbc, state, p);
+    }
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_t(const ssd_conv1d_args &a, const ConvParams &p, cudaStream_t st) {
+    switch (a.width) {
+        case 2: return launch_w<Tin, 2>(a, p, st);
+        case 3: return launch_w<Tin, 3>(a, p, st);
+        default: return launch_w<Tin, 4>(a, p, st);
+    }
+}
+
+}  // namespace
+
+cudaError_t conv1d_launch(const ssd_conv1d_args &a, bool decode, cudaStream_t st) {
+    ConvParams p;
+    p.T = a.total_tokens;
+    p.S = a.num_seqs;
+    p.K = decode ? 0 : a.num_chunks;
+    p.tpr = decode ? a.tokens_per_req : 0;
+    p.D = a.dim_x + 2 * a.dim_bc;
+    p.dim_x = a.dim_x;
+    p.dim_bc = a.dim_bc;
+    p.num_slots = a.num_slots;
+    p.null_id = a.null_block_id;
+    p.activation = a.activation;
+    p.decode = decode;
+    p.weight = a.weight;
+    p.bias = a.bias;
+    p.cu_seqlens = decode ? nullptr : a.cu_seqlens;
+    p.cu_chunk = decode ? nullptr : a.cu_chunk_seqlens;
+    p.last_chunk = decode ? nullptr : a.last_chunk_indices;
+    p.init_slot = a.init_slot;
+    p.out_slot = decode ? nullptr : a.out_slot;
+    p.chunk_slot = decode ? nullptr : a.chunk_slot;
+    p.err = a.err_word;
+    return a.dtype == SSD_BF16 ? launch_t<__nv_bfloat16>(a, p, st) : launch_t<float>(a, p, st);
+}
+
+}  // namespace ssd

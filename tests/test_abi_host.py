@@ -161,3 +161,47 @@ def test_decode_host_validation(lib, over, code):
 def test_empty_decode_is_a_no_op(lib):
     a = _decode_args(batch=0)
     assert lib.ssm_decode_update(ctypes.byref(a), None) == B.SSD_OK
+
+
+def _conv_args(**over):
+    a = B.Conv1dArgs()
+    a.total_tokens, a.num_seqs, a.num_chunks, a.tokens_per_req = 8, 2, 0, 4
+    a.dim_x, a.dim_bc, a.width, a.dtype, a.activation = 16, 8, 4, B.SSD_BF16, 1
+    a.num_slots, a.null_block_id = 4, 0
+    for f in ("xbc", "weight", "cu_seqlens", "x_out", "B_out", "C_out", "conv_state", "init_slot"):
+        setattr(a, f, 0x10000)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dim_x=12), B.SSD_ERR_INVALID_ARG),       # channels in groups of 8 (16-byte vectors)
+    (dict(width=5), B.SSD_ERR_INVALID_ARG),
+    (dict(width=1), B.SSD_ERR_INVALID_ARG),
+    (dict(activation=2), B.SSD_ERR_INVALID_ARG),
+    (dict(dtype=7), B.SSD_ERR_INVALID_ARG),
+    (dict(xbc=0x10008), B.SSD_ERR_INVALID_ARG),
+    (dict(cu_seqlens=None), B.SSD_ERR_INVALID_ARG),
+    (dict(conv_state=None), B.SSD_ERR_INVALID_ARG),  # slots without a state tensor
+    (dict(chunk_slot=0x10000), B.SSD_ERR_INVALID_ARG),  # chunk slots without chunk metadata
+])
+def test_conv1d_host_validation(lib, over, code):
+    a = _conv_args(**over)
+    assert lib.ssd_conv1d_varlen(ctypes.byref(a), None) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(tokens_per_req=3), B.SSD_ERR_INVALID_ARG),  # 2 requests x 3 tokens != 8 rows
+    (dict(tokens_per_req=0), B.SSD_ERR_INVALID_ARG),
+    (dict(init_slot=None), B.SSD_ERR_INVALID_ARG),   # decode needs the request slots
+])
+def test_conv1d_update_host_validation(lib, over, code):
+    a = _conv_args(**over)
+    assert lib.ssd_conv1d_update(ctypes.byref(a), None) == code
+
+
+def test_empty_conv1d_is_a_no_op(lib):
+    a = _conv_args(total_tokens=0, num_seqs=0)
+    assert lib.ssd_conv1d_varlen(ctypes.byref(a), None) == B.SSD_OK
+    assert lib.ssd_conv1d_update(ctypes.byref(a), None) == B.SSD_OK
