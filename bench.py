@@ -233,6 +233,48 @@ class Step:
         return h, h2d + meta_bytes, d2h
 
 
+def conv1d_leg(st, steps, warmup):
+    """The depthwise causal conv1d in front of the SSM (a next-row step, timed on its own, not
+    part of the step above) on the same prefill batch: xBC [T, H*P + 2*G*N] bf16 in, x/B/C out,
+    W = 4, conv states read at sequence starts and stored at every chunk end, as the SSM
+    states are.  Returns its line object."""
+    ssd = st.ssd
+    p = st.pre
+    T = int(p["cu_seqlens"][-1])
+    dim_x, dim_bc, W = st.H * st.P, st.G * st.N, 4
+    D = dim_x + 2 * dim_bc
+    g = torch.Generator(device=st.dev).manual_seed(11)
+    xbc = torch.randn(T, D, generator=g, device=st.dev).to(torch.bfloat16)
+    weight = 0.5 * torch.randn(D, W, generator=g, device=st.dev)
+    bias = 0.3 * torch.randn(D, generator=g, device=st.dev)
+    slots = p["cache"].shape[0]
+    state = torch.zeros(slots, W - 1, D, dtype=torch.bfloat16, device=st.dev)
+    m = st.device_meta(st.meta)
+    S = p["cu_seqlens"].numel() - 1
+    outs = st.ssd._binding._conv_outputs(xbc, dim_x, dim_bc, None, None, None)
+
+    def call():
+        ssd.ssd_conv1d_varlen(xbc, weight, st.cu_dev, dim_x, dim_bc, bias=bias, conv_state=state,
+                              init_slot=m["init_slot"][:S], chunk_slot=m["chunk_slot"][:st.K],
+                              cu_chunk_seqlens=m["cu_chunk_seqlens"], last_chunk_indices=m["last_chunk_indices"][:S],
+                              null_block_id=p["null_block_id"], x_out=outs[0], B_out=outs[1], C_out=outs[2])
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = 2 * T * D * 2 + st.K * (W - 1) * D * 2 + S * (W - 1) * D * 2 + D * (W + 1) * 4
+    hbm, _ = _peaks()
+    return {"what": "depthwise causal conv1d, W=4, silu, %d channels (x %d, B and C %d each)" % (D, dim_x, dim_bc),
+            "ms": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": nbytes,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "kernels": 2}
+
+
 def _barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
@@ -312,6 +354,7 @@ def gpu_arm(args, rank, world, dist_on):
         torch.cuda.synchronize()
         e2e_value, e2e_ms = job_rate(T + R, e0.elapsed_time(e1), args.steps, dist_on, dev)
 
+    conv = None if args.no_conv else conv1d_leg(st, args.steps, args.warmup)
     if rank != 0:
         return None
     hbm, peak_kind = _peaks()
@@ -339,6 +382,7 @@ def gpu_arm(args, rank, world, dist_on):
         "e2e": None if e2e_ms is None else {"value": e2e_value, "unit": UNIT,
                                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (st.prefill_kernels + (1 if R else 0)) * args.steps,
+        "conv1d": conv,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -417,6 +461,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="long_mixed", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiler runs)")
+    ap.add_argument("--no-conv", action="store_true", help="skip the conv1d measurement")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -22,10 +22,11 @@ template <typename T> __device__ __forceinline__ float ldg_f32(const T *p) { ret
 
 // Output gate: y * silu(z) = y * z * sigmoid(z) (the optional z argument of the
 // chunk-scan call on "[vllm] vLLM Mamba2 SSD 커널 웜업", section
-// "mamba_mixer2.py 변경 사항 (핵심)").  For z below about -88, __expf(-z) is
-// +inf and the quotient is the right limit, 0.
-__device__ __forceinline__ float silu_gate(float y, float z) { return y * (z / (1.f + __expf(-z))); }
-__device__ __forceinline__ float silu(float v) { return v / (1.f + __expf(-v)); }
+// "mamba_mixer2.py 변경 사항 (핵심)").  The quotient uses the fast approximate
+// divide (reciprocal times numerator, about 2 ulp): for z below about -88,
+// __expf(-z) is +inf, its reciprocal 0, and the result the right limit, 0.
+__device__ __forceinline__ float silu(float v) { return __fdividef(v, 1.f + __expf(-v)); }
+__device__ __forceinline__ float silu_gate(float y, float z) { return y * silu(z); }
 
 // ---- the per-token step size ----------------------------------------------
 // delta = clamp(softplus(dt + dt_bias), dt_min, dt_max).  softplus(v) is taken

@@ -13,7 +13,9 @@
 // channels (one 16-byte vector) and a run of kRun consecutive tokens, keeping
 // the W-1 previous inputs in registers as a sliding window, so every input is
 // read once from HBM (plus W-1 rows of overlap per run) and every output written
-// once, coalesced across the warp.  The outputs go straight to three tensors
+// once, coalesced across the warp.  The inputs of a batch of tokens are loaded
+// before any is used and the kernel is held to 4 CTAs per SM: together they
+// set how many bytes each SM keeps in flight, which is what bounds this kernel.  The outputs go straight to three tensors
 // (x, B, C), the layout the SSM calls take.  A second, small kernel then writes
 // the conv states at chunk ends and sequence ends: ordered after the first on
 // the stream, so all state reads precede all state writes.
@@ -23,7 +25,7 @@ namespace ssd {
 namespace {
 
 constexpr int kVec = 8;        // channels per thread (16 bytes of bf16)
-constexpr int kRun = 16;       // tokens per thread
+constexpr int kRun = 64;       // tokens per thread (amortises the taps and the history reads)
 constexpr int kConvThreads = 128;
 
 struct ConvParams {
@@ -36,6 +38,17 @@ struct ConvParams {
 
 template <typename T> struct Vec8;
 template <> struct Vec8<__nv_bfloat16> {
+    static constexpr int kBatch = 8;  // tokens whose inputs are loaded before any is used
+    struct Raw { uint4 u; };
+    static __device__ __forceinline__ Raw load_raw(const __nv_bfloat16 *p) { return {*reinterpret_cast<const uint4 *>(p)}; }
+    static __device__ __forceinline__ void unpack(const Raw &r, float (&v)[kVec]) {
+        const uint32_t w[4] = {r.u.x, r.u.y, r.u.z, r.u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
     static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[kVec]) {
         const uint4 u = *reinterpret_cast<const uint4 *>(p);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -60,6 +73,15 @@ template <> struct Vec8<__nv_bfloat16> {
     }
 };
 template <> struct Vec8<float> {
+    static constexpr int kBatch = 4;
+    struct Raw { float4 a, b; };
+    static __device__ __forceinline__ Raw load_raw(const float *p) {
+        return {reinterpret_cast<const float4 *>(p)[0], reinterpret_cast<const float4 *>(p)[1]};
+    }
+    static __device__ __forceinline__ void unpack(const Raw &r, float (&v)[kVec]) {
+        v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w;
+        v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
+    }
     static __device__ __forceinline__ void load(const float *p, float (&v)[kVec]) {
         const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
@@ -117,8 +139,10 @@ __device__ __forceinline__ void input_before(const Tin *xbc, const Tin *state, i
 }
 
 template <typename Tin, int W>
-__global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const Tin *__restrict__ xbc, const Tin *state,
-                                                              Tin *x_out, Tin *B_out, Tin *C_out, ConvParams p) {
+__global__ void __launch_bounds__(kConvThreads, 4) conv1d_kernel(const Tin *__restrict__ xbc,
+                                                              const Tin *__restrict__ state, Tin *__restrict__ x_out,
+                                                              Tin *__restrict__ B_out, Tin *__restrict__ C_out,
+                                                              ConvParams p) {
     const int vec = blockIdx.x * kConvThreads + threadIdx.x;
     const int t0 = blockIdx.y * kRun;
     if (vec * kVec >= p.D || t0 >= p.T) return;
@@ -147,39 +171,51 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const Tin *__restr
     float win[W - 1][kVec];  // win[0] oldest
 #pragma unroll
     for (int j = 0; j < W - 1; ++j) input_before<Tin, W>(xbc, state, hslot, p.D, s0, t0 - (W - 1) + j, c0, win[j]);
-    for (int t = t0; t < t1; ++t) {
-        if (t >= e0) {  // next sequence (empty ones have no tokens to visit)
-            do {
-                if (r + 1 >= p.S) {  // cu_seqlens does not end at T
-                    if (vec == 0) report(p.err, SSD_DEVERR_METADATA);
-                    return;
-                }
-                ++r;
-                s0 = seq_start(p, r);
-                e0 = seq_end(p, r);
-            } while (e0 <= t);
-            hslot = history_slot(p, r, vec == 0);
+    constexpr int kB = Vec8<Tin>::kBatch;
+    for (int tb = t0; tb < t1; tb += kB) {
+        // the batch's inputs first: kB independent 16-byte loads in flight per thread
+        typename Vec8<Tin>::Raw raw[kB];
 #pragma unroll
-            for (int j = 0; j < W - 1; ++j) input_before<Tin, W>(xbc, state, hslot, p.D, s0, t - (W - 1) + j, c0, win[j]);
+        for (int j = 0; j < kB; ++j)
+            if (tb + j < t1) raw[j] = Vec8<Tin>::load_raw(xbc + (size_t)(tb + j) * p.D + c0);
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int t = tb + j;
+            if (t >= t1) break;
+            if (t >= e0) {  // next sequence (empty ones have no tokens to visit)
+                do {
+                    if (r + 1 >= p.S) {  // cu_seqlens does not end at T
+                        if (vec == 0) report(p.err, SSD_DEVERR_METADATA);
+                        return;
+                    }
+                    ++r;
+                    s0 = seq_start(p, r);
+                    e0 = seq_end(p, r);
+                } while (e0 <= t);
+                hslot = history_slot(p, r, vec == 0);
+#pragma unroll
+                for (int jj = 0; jj < W - 1; ++jj)
+                    input_before<Tin, W>(xbc, state, hslot, p.D, s0, t - (W - 1) + jj, c0, win[jj]);
+            }
+            float cur[kVec];
+            Vec8<Tin>::unpack(raw[j], cur);
+            float o[kVec];
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) {
+                float acc = b[i];
+#pragma unroll
+                for (int k = 0; k < W - 1; ++k) acc = fmaf(w[k][i], win[k][i], acc);
+                acc = fmaf(w[W - 1][i], cur[i], acc);
+                o[i] = p.activation ? silu(acc) : acc;
+            }
+            if (hslot != -2) Vec8<Tin>::store(out + (size_t)t * ostride + ocol, o);
+#pragma unroll
+            for (int jj = 0; jj + 1 < W - 1; ++jj)
+#pragma unroll
+                for (int i = 0; i < kVec; ++i) win[jj][i] = win[jj + 1][i];
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) win[W - 2][i] = cur[i];
         }
-        float cur[kVec];
-        Vec8<Tin>::load(xbc + (size_t)t * p.D + c0, cur);
-        float o[kVec];
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) {
-            float acc = b[i];
-#pragma unroll
-            for (int k = 0; k < W - 1; ++k) acc = fmaf(w[k][i], win[k][i], acc);
-            acc = fmaf(w[W - 1][i], cur[i], acc);
-            o[i] = p.activation ? silu(acc) : acc;
-        }
-        if (hslot != -2) Vec8<Tin>::store(out + (size_t)t * ostride + ocol, o);
-#pragma unroll
-        for (int j = 0; j + 1 < W - 1; ++j)
-#pragma unroll
-            for (int i = 0; i < kVec; ++i) win[j][i] = win[j + 1][i];
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) win[W - 2][i] = cur[i];
     }
 }
 
