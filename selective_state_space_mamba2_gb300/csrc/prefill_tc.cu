@@ -32,7 +32,8 @@
 //   warps 4-7  "consumer" warpgroup: state update, the fp16 state tile for
 //              the next block's M3, the chunk-boundary stores, y and its
 //              coalesced copy-out
-//   warp 8     TMA producer, C/B/x tiles double-buffered (128-byte swizzle)
+//   warp 8     TMA producer: C/B tiles in two stages, x tiles in three (128-byte
+//              swizzle)
 //   warp 9     TMEM allocation (512 columns) and MMA issue
 // Thread t of a warpgroup owns TMEM lane t: token row t of S, Y1, Y2 and
 // dstate row t of dS and of the state.  Every mbarrier wait is bounded; on a
@@ -100,8 +101,8 @@ enum {
     S_RDY0, S_RDY1,                                    // S of the block, per S buffer
     OPS_W,     // producer wg: w x and fp16 x of the block are in smem          (4 arrivals)
     PRDY0, PRDY1,  // producer wg: P of the block is in TMEM, per S buffer          (4)
-                   // (one barrier per buffer: M1 of the next block goes out before M2 of this
-                   // one, so the P pass can run two blocks ahead of the MMA warp's wait)
+                   // (one barrier per buffer keeps each waiter within one phase of its
+                   // barrier whichever order M1 of the next block and M2 of this one go out in)
     OPS_H,     // consumer wg: fp16 state entering the block is in smem         (4)
     DS_FREE,   // consumer wg: read dS of the previous block                    (4)
     Y1_FREE,   // consumer wg: read Y1 of the previous block                    (4)
@@ -321,35 +322,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdS = idesc_f16(128, 128, 0, 0);
             constexpr uint32_t kIdY = idesc_f16(128, 64, 0, 1);
             constexpr uint32_t kIdD = idesc_f16(128, 64, 1, 1);
-            const uint32_t aXW = smem_u32(sXW), aH = smem_u32(sH);
+            // Tile descriptors, built once: a K slice is desc_at(tile, its byte offset), so the
+            // issue of each MMA waits on nothing but the previous one.
+            const uint64_t dC0 = sw128_desc(smem_u32(stage_c(0)), 16, 1024), dC1 = sw128_desc(smem_u32(stage_c(1)), 16, 1024);
+            const uint64_t dBk0 = sw128_desc(smem_u32(stage_b(0)), 16, 1024), dBk1 = sw128_desc(smem_u32(stage_b(1)), 16, 1024);
+            const uint64_t dBm0 = sw128_desc(smem_u32(stage_b(0)), 16384, 1024);
+            const uint64_t dBm1 = sw128_desc(smem_u32(stage_b(1)), 16384, 1024);
+            const uint64_t dX0 = sw128_desc(smem_u32(stage_x(0)), 1024, 1024), dX1 = sw128_desc(smem_u32(stage_x(1)), 1024, 1024),
+                           dX2 = sw128_desc(smem_u32(stage_x(2)), 1024, 1024);
+            const uint64_t dH = sw128_desc(smem_u32(sH), 1024, 1024), dXW = sw128_desc(smem_u32(sXW), 1024, 1024);
             auto issue_m1 = [&](int b) {
                 const int sb = b & 1;
-                const uint32_t aC = smem_u32(stage_c(sb)), aB = smem_u32(stage_b(sb));
+                const uint64_t da = sb ? dC1 : dC0, db = sb ? dBk1 : dBk0;
+                const uint32_t dS = tm + (sb ? COL_S1 : COL_S0);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_ss(tm + (sb ? COL_S1 : COL_S0), sw128_desc(aC + ko, 16, 1024), sw128_desc(aB + ko, 16, 1024),
-                           kIdS, k > 0);
+                    mma_ss(dS, desc_at(da, ko), desc_at(db, ko), kIdS, k > 0);
                 }
                 mma_commit(&bar[S_RDY0 + sb]);
             };
             bool ok = mbar_wait(&bar[FULL_CB0], 0);
-            int m1_issued = 0;
             if (ok) {
                 tc_fence_after();
                 issue_m1(0);
-                m1_issued = 1;
             }
+            // Per block, in this order: M4 (the state update waits on it), M3, M2 (y), then M1 of
+            // the next block, whose S is needed only after the next block's scan and w x.
             for (int i = 0; ok && i < nblocks; ++i) {
-                const int s = i & 1;
-                const uint32_t aC = smem_u32(stage_c(s)), aB = smem_u32(stage_b(s)), aX = smem_u32(stage_x(i));
+                const int s = i & 1, xs = i % kXStages;
+                const uint64_t dCs = s ? dC1 : dC0, dBms = s ? dBm1 : dBm0;
+                const uint64_t dXs = xs == 0 ? dX0 : (xs == 1 ? dX1 : dX2);
                 // M4: dS = B^T (w x) once w x exists and dS of the previous block was read
                 if (!(ok = mbar_wait(&bar[OPS_W], i & 1)) || !(ok = mbar_wait(&bar[DS_FREE], i & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_ss(tm + COL_DS, sw128_desc(aB + 2048 * k, 16384, 1024), sw128_desc(aXW + 2048 * k, 1024, 1024),
-                           kIdD, k > 0);
+                    mma_ss(tm + COL_DS, desc_at(dBms, 2048 * k), desc_at(dXW, 2048 * k), kIdD, k > 0);
                 mma_commit(&bar[ACC_DS]);
                 // M3: Y2 = C Hprev^T once the state entering the block exists
                 if (!(ok = mbar_wait(&bar[OPS_H], i & 1))) break;
@@ -357,38 +366,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_ss(tm + COL_Y2 + 64 * s, sw128_desc(aC + ko, 16, 1024), sw128_desc(aH + 2048 * k, 1024, 1024),
-                           kIdY, k > 0);
+                    mma_ss(tm + COL_Y2 + 64 * s, desc_at(dCs, ko), desc_at(dH, 2048 * k), kIdY, k > 0);
                 }
                 mma_commit(&bar[H_FREE]);
                 mma_commit(&bar[EMPTY_CB0 + s]);  // M1, M4 and M3 of the block have read its C/B stage
-                // M2 when P is ready (and Y1 was read); M1 of the next block as soon as its tiles land
-                const long long t0 = clock64();
-                for (;;) {
-                    if (m1_issued == i + 1 && i + 1 < nblocks &&
-                        mbar_try_wait(&bar[FULL_CB0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1)) {
-                        tc_fence_after();
-                        issue_m1(i + 1);
-                        ++m1_issued;
-                    }
-                    if (mbar_try_wait(&bar[PRDY0 + s], (i >> 1) & 1) && mbar_try_wait(&bar[Y1_FREE], i & 1)) break;
-                    if (clock64() - t0 > 2000000000ll) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!ok) break;
+                // M2: Y1 = P X once P is ready and Y1 of the previous block was read
+                if (!(ok = mbar_wait(&bar[PRDY0 + s], (i >> 1) & 1)) || !(ok = mbar_wait(&bar[Y1_FREE], i & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_ts(tm + COL_Y1, tm + (s ? COL_S1 : COL_S0) + 8 * k, sw128_desc(aX + 2048 * k, 1024, 1024), kIdY,
-                           k > 0);
+                    mma_ts(tm + COL_Y1, tm + (s ? COL_S1 : COL_S0) + 8 * k, desc_at(dXs, 2048 * k), kIdY, k > 0);
                 mma_commit(&bar[ACC_Y]);
-                if (m1_issued == i + 1 && i + 1 < nblocks) {
+                if (i + 1 < nblocks) {
                     if (!(ok = mbar_wait(&bar[FULL_CB0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1))) break;
                     tc_fence_after();
                     issue_m1(i + 1);
-                    ++m1_issued;
                 }
             }
             if (!ok) report(p.err, SSD_DEVERR_TIMEOUT);

@@ -189,6 +189,15 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
     return d;
 }
 
+// The descriptor of the same tile `byte_off` bytes further on.  The address
+// field (bits 0-13, address >> 4) of a shared-memory descriptor cannot carry
+// into the next field (shared memory is below 256 KB), so this is one 32-bit
+// add on the low word.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t byte_off) {
+    const uint32_t lo = (uint32_t)d + (byte_off >> 4);
+    return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
 // A/B major-ness (0 = K-major, 1 = MN-major), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
