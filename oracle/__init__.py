@@ -64,6 +64,11 @@ def _load():
             ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
             ctypes.c_int32, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int32, ctypes.c_double,
             ctypes.c_double, ip, ctypes.c_int32, ip, dp, up, dp, dp, dp, ctypes.c_int32]
+        lib.oracle_mamba1_prefill.restype = ctypes.c_int
+        lib.oracle_mamba1_prefill.argtypes = [
+            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            dp, dp, dp, dp, dp, dp, dp, ctypes.c_int32, ctypes.c_double, ctypes.c_double,
+            ip, ctypes.c_int32, ip, dp, up, dp, dp, dp, ctypes.c_int32]
         lib.oracle_chunk_metadata.restype = ctypes.c_int32
         lib.oracle_chunk_metadata.argtypes = [ctypes.c_int32, ctypes.c_int32, ip, ip,
                                               ctypes.c_int32, ip, ip, ip, ip]
@@ -408,3 +413,120 @@ def causal_conv1d_with_cache(xbc, weight, bias, cu_seqlens, cache, init_slot, ou
             if int(out_slot[r]) != null_block_id:
                 new[int(out_slot[r])] = final[r]
     return out, new
+
+
+# ---------------------------------------------------------------- Mamba1 ----
+# The selective scan of the Mamba paper (S6) that "[vLLM] Mamba (SSM): 선형 시간
+# 복잡도 시퀀스 모델링" summarises in "논문 핵심 내용": every channel d carries
+# its own state vector s[d, :] of dstate values with its own decay rates
+# A[d, :]; Delta, B and C depend on the token.  Mamba1 has no chunk of its own
+# ("[vllm] vLLM Mamba2 SSD 커널 웜업", "vllm/config/model.py 변경 사항": the
+# default chunk size becomes 2048); chunks only decide where states are taken
+# out for prefix caching, exactly as for Mamba2.
+
+
+def mamba1_prefill(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens=None, D=None, dt_bias=None,
+                   initial_states=None, has_initial_states=None, dt_softplus=True,
+                   dt_limit=(0.0, math.inf), nthreads=None, z=None):
+    """Sequential fp64 Mamba1 recurrence over packed varlen sequences.
+
+    x and dt [T,Dc], A [Dc,N], B and C [T,G,N], D and dt_bias [Dc],
+    initial_states [S,Dc,N].  Returns ``(y [T,Dc], chunk_states [K,Dc,N] or
+    None, final_states [S,Dc,N])``; with a gate z [T,Dc], y is y * silu(z).
+    """
+    x = _f64(x); dt = _f64(dt); A = _f64(A); B = _f64(B); C = _f64(C)
+    D = _f64(D); dt_bias = _f64(dt_bias)
+    cu = _i32(cu_seqlens)
+    T, Dc = x.shape
+    G, N = B.shape[1], B.shape[2]
+    S = cu.shape[0] - 1
+    assert dt.shape == (T, Dc) and B.shape == (T, G, N) and C.shape == (T, G, N) and A.shape == (Dc, N)
+    cc = _i32(cu_chunk_seqlens)
+    K = 0 if cc is None else cc.shape[0] - 1
+    init = _f64(initial_states)
+    has = None
+    if init is not None:
+        assert init.shape == (S, Dc, N)
+        has = np.ones(S, np.uint8) if has_initial_states is None else \
+            np.ascontiguousarray(np.asarray(has_initial_states, dtype=bool), dtype=np.uint8)
+    y = np.empty((T, Dc), np.float64)
+    cs = np.empty((K, Dc, N), np.float64) if K > 0 else None
+    fs = np.empty((S, Dc, N), np.float64)
+    rc = _load().oracle_mamba1_prefill(
+        T, S, Dc, N, G, _ptr(x, ctypes.c_double), _ptr(dt, ctypes.c_double), _ptr(B, ctypes.c_double),
+        _ptr(C, ctypes.c_double), _ptr(A, ctypes.c_double), _ptr(D, ctypes.c_double),
+        _ptr(dt_bias, ctypes.c_double), int(bool(dt_softplus)), float(dt_limit[0]), float(dt_limit[1]),
+        _ptr(cu, ctypes.c_int32), K, _ptr(cc, ctypes.c_int32), _ptr(init, ctypes.c_double),
+        _ptr(has, ctypes.c_uint8), _ptr(y, ctypes.c_double), _ptr(cs, ctypes.c_double),
+        _ptr(fs, ctypes.c_double), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_mamba1_prefill rejected its arguments (code %d)" % rc)
+    if z is not None:
+        zz = _f64(z)
+        assert zz.shape == (T, Dc)
+        y = y * silu(zz)
+    return y, cs, fs
+
+
+def mamba1_prefill_with_cache(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, init_slot, chunk_slot,
+                              null_block_id, cache, D=None, dt_bias=None, dt_softplus=True,
+                              dt_limit=(0.0, math.inf), nthreads=None, z=None):
+    """mamba1_prefill against a state cache [slots,Dc,N]: initial states are
+    read before any write; chunk end states go to their slots unless null.
+    Returns ``(y, new_cache)``."""
+    S = len(init_slot)
+    Dc, N = cache.shape[1:]
+    init = np.zeros((S, Dc, N), np.float64)
+    has = np.zeros(S, bool)
+    for r in range(S):
+        if int(init_slot[r]) != null_block_id:
+            init[r] = cache[int(init_slot[r])]
+            has[r] = True
+    y, cs, _ = mamba1_prefill(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, D=D, dt_bias=dt_bias,
+                              initial_states=init, has_initial_states=has, dt_softplus=dt_softplus,
+                              dt_limit=dt_limit, nthreads=nthreads, z=z)
+    new_cache = np.array(cache, dtype=np.float64, copy=True)
+    for k in range(len(chunk_slot)):
+        if int(chunk_slot[k]) != null_block_id:
+            new_cache[int(chunk_slot[k])] = cs[k]
+    return y, new_cache
+
+
+def mamba1_decode_with_cache(x, dt, A, B, C, state_indices, num_accepted_tokens, null_block_id, cache,
+                             D=None, dt_bias=None, dt_softplus=True, dt_limit=(0.0, math.inf),
+                             nthreads=None, z=None):
+    """Mamba1 decode against a cache [slots,Dc,N], with the routing of
+    ``decode_with_cache``: request r resumes from column num_accepted[r] of
+    its state-index row, skips if that slot is null, and the state after its
+    token k goes to column k unless null.  Returns ``(y, live, new_cache)``;
+    y rows of requests that are not live are NaN."""
+    si = np.asarray(state_indices)
+    R = si.shape[0]
+    x64 = _f64(x)
+    T, Dc = x64.shape
+    tpr = T // R
+    assert tpr * R == T
+    N = cache.shape[2]
+    rd = decode_read_slots(si, num_accepted_tokens, null_block_id)
+    live = rd != null_block_id
+    read = np.zeros((R, Dc, N), np.float64)
+    for r in range(R):
+        if live[r]:
+            read[r] = cache[int(rd[r])]
+    cu = np.arange(0, T + 1, tpr, dtype=np.int32)
+    cc = np.arange(0, T + 1, dtype=np.int32)
+    y, cs, _ = mamba1_prefill(x64, dt, A, B, C, cu, cc, D=D, dt_bias=dt_bias, initial_states=read,
+                              has_initial_states=np.ones(R, bool), dt_softplus=dt_softplus,
+                              dt_limit=dt_limit, nthreads=nthreads, z=z)
+    states = cs.reshape(R, tpr, Dc, N)
+    y = y.reshape(R, tpr, Dc)
+    y[~live] = np.nan
+    new_cache = np.array(cache, dtype=np.float64, copy=True)
+    for r in range(R):
+        if not live[r]:
+            continue
+        for k in range(tpr):
+            ws = int(si[r, k])
+            if ws != null_block_id:
+                new_cache[ws] = states[r, k]
+    return y.reshape(T, Dc), live, new_cache

@@ -213,3 +213,128 @@ int32_t oracle_chunk_metadata(int32_t S, int32_t chunk_size, const int32_t *cu_s
     cu_chunk_seqlens[k] = cu_seqlens[S];
     return k;
 }
+
+/*
+ * Mamba1 selective scan (S6), per-channel state.
+ *
+ * What it follows
+ *   [vLLM] Mamba (SSM): 선형 시간 복잡도 시퀀스 모델링, section "논문 핵심 내용":
+ *     S6 makes Delta, B and C functions of the input, where S4 kept them
+ *     fixed; the state of each channel is a vector of dstate values.
+ *   [vllm] vLLM Mamba2 SSD 커널 웜업, section "vllm/config/model.py 변경 사항":
+ *     Mamba1 has no chunk of its own; the default chunk size (2048) is the
+ *     granularity at which states are taken out for prefix caching.
+ * Readings where the pages are silent (the Mamba paper's S6): A is a real
+ * [channels, dstate] matrix (one decay rate per channel and state index),
+ * Delta is per (token, channel) with the same softplus/clamp as Mamba2, B and
+ * C are [T, G, dstate] shared by the channels of a group (G = 1 in Mamba1),
+ * D and dt_bias are per channel.  Evaluated token by token in fp64:
+ *   delta = clamp(softplus(dt[t,d] + dt_bias[d]), dt_min, dt_max)
+ *   s[d,n] <- exp(delta * A[d,n]) * s[d,n] + delta * x[t,d] * B[t,g,n]
+ *   y[t,d] = sum_n C[t,g,n] * s[d,n] + D[d] * x[t,d],   g = d / (channels / G)
+ * and the running state of every channel is emitted after the last token of
+ * every chunk.
+ */
+typedef struct {
+    int64_t T;
+    int32_t S, Dc, N, G;
+    const double *x, *dt, *B, *C, *A, *Dskip, *dt_bias;
+    int dt_softplus;
+    double dt_min, dt_max;
+    const int32_t *cu_seqlens;
+    const int32_t *chunk_of_end_token;
+    const double *init_states; /* [S,Dc,N] or NULL */
+    const uint8_t *has_init;
+    double *y;                 /* [T,Dc] */
+    double *chunk_states;      /* [K,Dc,N] or NULL */
+    double *final_states;      /* [S,Dc,N] or NULL */
+    int32_t nthreads, tid;
+} oracle_m1_job;
+
+static void oracle_m1_unit(const oracle_m1_job *j, int32_t r, int32_t d, double *s) {
+    const int32_t N = j->N, Dc = j->Dc, G = j->G;
+    const int32_t g = d / (Dc / G);
+    const size_t off = (size_t)d * N;
+    if (j->init_states && j->has_init && j->has_init[r])
+        memcpy(s, j->init_states + (size_t)r * Dc * N + off, (size_t)N * sizeof(double));
+    else
+        memset(s, 0, (size_t)N * sizeof(double));
+    const double *Ad = j->A + off;
+    const double Dd = j->Dskip ? j->Dskip[d] : 0.0;
+    const double bias = j->dt_bias ? j->dt_bias[d] : 0.0;
+    for (int64_t t = j->cu_seqlens[r]; t < j->cu_seqlens[r + 1]; ++t) {
+        const double delta = oracle_delta(j->dt[t * Dc + d], bias, j->dt_softplus, j->dt_min, j->dt_max);
+        const double xt = j->x[t * Dc + d];
+        const double *Bt = j->B + ((size_t)t * G + g) * N;
+        const double *Ct = j->C + ((size_t)t * G + g) * N;
+        double acc = 0.0;
+        for (int32_t n = 0; n < N; ++n) {
+            s[n] = exp(delta * Ad[n]) * s[n] + delta * xt * Bt[n];
+            acc += Ct[n] * s[n];
+        }
+        j->y[t * Dc + d] = acc + Dd * xt;
+        const int32_t k = j->chunk_of_end_token ? j->chunk_of_end_token[t] : -1;
+        if (k >= 0 && j->chunk_states)
+            memcpy(j->chunk_states + (size_t)k * Dc * N + off, s, (size_t)N * sizeof(double));
+    }
+    if (j->final_states)
+        memcpy(j->final_states + (size_t)r * Dc * N + off, s, (size_t)N * sizeof(double));
+}
+
+static void *oracle_m1_worker(void *arg) {
+    const oracle_m1_job *j = (const oracle_m1_job *)arg;
+    double *s = (double *)malloc((size_t)j->N * sizeof(double));
+    if (!s) return (void *)1;
+    const int64_t units = (int64_t)j->S * j->Dc;
+    for (int64_t u = j->tid; u < units; u += j->nthreads)
+        oracle_m1_unit(j, (int32_t)(u / j->Dc), (int32_t)(u % j->Dc), s);
+    free(s);
+    return NULL;
+}
+
+/* Varlen Mamba1 scan; arguments and return codes as oracle_ssd_prefill, with
+ * x, dt [T,Dc], A [Dc,N], D and dt_bias [Dc], states [.,Dc,N]. */
+int oracle_mamba1_prefill(int64_t T, int32_t S, int32_t Dc, int32_t N, int32_t G,
+                          const double *x, const double *dt, const double *B, const double *C,
+                          const double *A, const double *Dskip, const double *dt_bias,
+                          int32_t dt_softplus, double dt_min, double dt_max,
+                          const int32_t *cu_seqlens, int32_t K, const int32_t *cu_chunk_seqlens,
+                          const double *init_states, const uint8_t *has_init,
+                          double *y, double *chunk_states, double *final_states, int32_t nthreads) {
+    if (T < 0 || S < 0 || Dc <= 0 || N <= 0 || G <= 0 || Dc % G != 0) return -1;
+    if (cu_seqlens[0] != 0 || cu_seqlens[S] != T) return -2;
+    for (int32_t r = 0; r < S; ++r)
+        if (cu_seqlens[r + 1] < cu_seqlens[r]) return -2;
+    int32_t *end_chunk = NULL;
+    if (K > 0) {
+        if (!cu_chunk_seqlens || cu_chunk_seqlens[0] != 0 || cu_chunk_seqlens[K] != T) return -3;
+        end_chunk = (int32_t *)malloc((size_t)(T > 0 ? T : 1) * sizeof(int32_t));
+        if (!end_chunk) return -4;
+        for (int64_t t = 0; t < T; ++t) end_chunk[t] = -1;
+        for (int32_t k = 0; k < K; ++k) {
+            if (cu_chunk_seqlens[k + 1] <= cu_chunk_seqlens[k]) { free(end_chunk); return -3; }
+            end_chunk[cu_chunk_seqlens[k + 1] - 1] = k;
+        }
+    }
+    if (nthreads < 1) nthreads = 1;
+    oracle_m1_job *jobs = (oracle_m1_job *)malloc((size_t)nthreads * sizeof(oracle_m1_job));
+    pthread_t *th = (pthread_t *)malloc((size_t)nthreads * sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); free(end_chunk); return -4; }
+    oracle_m1_job base = {T, S, Dc, N, G, x, dt, B, C, A, Dskip, dt_bias, dt_softplus, dt_min, dt_max,
+                          cu_seqlens, end_chunk, init_states, has_init, y, chunk_states, final_states,
+                          nthreads, 0};
+    int rc = 0;
+    for (int32_t i = 0; i < nthreads; ++i) {
+        jobs[i] = base;
+        jobs[i].tid = i;
+        if (i > 0 && pthread_create(&th[i], NULL, oracle_m1_worker, &jobs[i]) != 0) { rc = -5; nthreads = i; break; }
+    }
+    if (oracle_m1_worker(&jobs[0]) != NULL) rc = -4;
+    for (int32_t i = 1; i < nthreads; ++i) {
+        void *ret = NULL;
+        pthread_join(th[i], &ret);
+        if (ret != NULL) rc = -4;
+    }
+    free(jobs); free(th); free(end_chunk);
+    return rc;
+}

@@ -86,3 +86,31 @@ def rel_err(a, b):
     b = np.asarray(b, np.float64)
     rms = np.sqrt(np.mean(b * b)) if b.size else 0.0
     return float(np.max(np.abs(a - b)) / max(rms, 1e-300)) if a.size else 0.0
+
+
+def mamba1_quadratic(x, delta, A, B, C, D, h0):
+    """Mamba1 (per-channel state) in matrix form, one segment with starting
+    state h0 [Dc,N].  For channel d and state index n, with c = A[d,n] *
+    cumsum(delta[:, d]):
+      s_t[d,n] = sum_{s<=t} exp(c_t - c_s) delta_s[d] B_s[g,n] x_s[d] + exp(c_t) h0[d,n]
+      y_t[d]   = sum_n C_t[g,n] s_t[d,n] + D[d] x_t[d]
+    Returns y [L,Dc] and the end state [Dc,N]."""
+    L, Dc = x.shape
+    G, N = B.shape[1], B.shape[2]
+    grp = np.repeat(np.arange(G), Dc // G)
+    y = np.zeros((L, Dc))
+    end = np.zeros((Dc, N))
+    mask = np.tril(np.ones((L, L), dtype=bool))
+    for d in range(Dc):
+        g = grp[d]
+        cd = np.cumsum(delta[:, d])
+        u = delta[:, d] * x[:, d]
+        for n in range(N):
+            c = A[d, n] * cd
+            decay = np.where(mask, np.exp(c[:, None] - c[None, :]), 0.0)
+            s = decay @ (u * B[:, g, n]) + np.exp(c) * h0[d, n]
+            y[:, d] += C[:, g, n] * s
+            end[d, n] = s[-1]
+        if D is not None:
+            y[:, d] += D[d] * x[:, d]
+    return y, end
