@@ -8,6 +8,10 @@
  *   ssd_prefill_varlen  device: chunked SSD prefill scan over packed sequences
  *   ssm_decode_update   device: single/speculative-token decode state update
  *
+ * Next to them: the depthwise causal conv1d that produces x, B and C
+ * (ssd_conv1d_varlen / ssd_conv1d_update) and the Mamba1 selective scan with
+ * per-channel states (mamba1_scan_varlen / mamba1_state_update).
+ *
  * The recurrence (per head h, group g = h / (nheads / ngroups)):
  *   delta_t = clamp(softplus(dt[t,h] + dt_bias[h]), dt_min, dt_max)
  *   s_t     = exp(delta_t * A[h]) * s_{t-1} + delta_t * x[t,h,:] (outer) B[t,g,:]
@@ -363,6 +367,78 @@ SSD_API ssd_status_t ssd_conv1d_varlen(const ssd_conv1d_args *args, ssd_stream_t
  * cu_chunk_seqlens, last_chunk_indices, out_slot and chunk_slot are ignored.
  */
 SSD_API ssd_status_t ssd_conv1d_update(const ssd_conv1d_args *args, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Mamba1 selective scan (device)
+ *
+ * The S6 layer of the Mamba paper as "[vLLM] Mamba (SSM): 선형 시간 복잡도
+ * 시퀀스 모델링" summarises it in "논문 핵심 내용": Delta, B and C are
+ * functions of the token, and every channel d keeps its own state vector
+ * s[d, 0..N-1] with its own decay rates A[d, n] (Mamba2 ties the rate to the
+ * head).  Per channel d, group g = d / (dim / ngroups):
+ *   delta   = clamp(softplus(dt[t,d] + dt_bias[d]), dt_min, dt_max)
+ *   s[d,n] <- exp(delta * A[d,n]) * s[d,n] + delta * x[t,d] * B[t,g,n]
+ *   y[t,d]  = sum_n C[t,g,n] * s[d,n] + D[d] * x[t,d]   (then y * silu(z[t,d]) if z)
+ * Mamba1 has no chunk of its own; prefix caching takes the state out every
+ * chunk_size tokens, 2048 by default for Mamba1 ("[vllm] vLLM Mamba2 SSD 커널
+ * 웜업", "vllm/config/model.py 변경 사항").  The chunk metadata and slot
+ * routing are those of ssd_chunk_metadata, and decode follows the same
+ * state-index, padding and speculative-token rules as ssm_decode_update.
+ * ------------------------------------------------------------------------ */
+typedef struct mamba1_args {
+    int32_t total_tokens;   /* T (mamba1_state_update: batch * tokens_per_req) */
+    int32_t num_seqs;       /* S (mamba1_state_update: batch R, rows of state_indices) */
+    int32_t num_chunks;     /* K (mamba1_scan_varlen) */
+    int32_t tokens_per_req; /* mamba1_state_update: 1 + num_speculative_tokens */
+    int32_t dim;            /* channels Dc (d_inner), a multiple of 64 */
+    int32_t dstate;         /* N, 8 or 16 */
+    int32_t ngroups;        /* G; dim / G is a multiple of 64 (Mamba1: G = 1) */
+    int32_t dtype;          /* ssd_dtype_t of x, dt, B, C, z and y */
+    int32_t dt_softplus;
+    float dt_min, dt_max;
+    int32_t num_slots;
+    int32_t null_block_id;
+    int32_t state_indices_cols; /* mamba1_state_update: columns of a state_indices row */
+    /* device pointers */
+    const void *x;  /* [T, Dc], 16-byte aligned */
+    const void *dt; /* [T, Dc], 16-byte aligned */
+    const void *B;  /* [T, G, N], 16-byte aligned */
+    const void *C;  /* [T, G, N], 16-byte aligned */
+    const void *z;  /* [T, Dc] or NULL, 16-byte aligned: output gate */
+    const float *A; /* [Dc, N] */
+    const float *D; /* [Dc] or NULL */
+    const float *dt_bias;              /* [Dc] or NULL */
+    const int32_t *cu_seqlens;         /* scan: [S+1] */
+    const int32_t *cu_chunk_seqlens;   /* scan: [K+1] */
+    const int32_t *last_chunk_indices; /* scan: [S] */
+    const int32_t *init_slot;          /* scan: [S] or NULL */
+    const int32_t *chunk_slot;         /* scan: [K] or NULL */
+    const int32_t *state_indices;      /* update: [R, state_indices_cols] */
+    const int32_t *num_accepted_tokens; /* update: [R] or NULL */
+    float *state_cache;                /* [num_slots, Dc, N] fp32, 16-byte aligned */
+    void *y;                           /* [T, Dc], 16-byte aligned */
+    uint32_t *err_word;                /* device word or NULL */
+} mamba1_args;
+
+/*
+ * Varlen prefill over packed sequences: sequence r starts from
+ * state_cache[init_slot[r]] (zeros when null or when init_slot is NULL), and
+ * the state after the last token of chunk k goes to chunk_slot[k] unless null.
+ * All reads of a sequence's initial state happen before its first write.
+ * Host checks: sizes, dim % 64 == 0, (dim / ngroups) % 64 == 0, dstate in
+ * {8, 16}, pointers and alignments; SSD_ERR_CUDA if the launch fails.  One
+ * kernel.
+ */
+SSD_API ssd_status_t mamba1_scan_varlen(const mamba1_args *args, ssd_stream_t stream);
+
+/*
+ * Decode: request r resumes from state_indices[r, num_accepted_tokens[r]]
+ * (padding when that id is null: nothing of r is read or written), applies its
+ * tokens_per_req tokens in order, writes y for each and stores the state after
+ * token k to state_indices[r, k] unless null.  Host checks as for the scan,
+ * plus tokens_per_req >= 1 and state_indices_cols >= tokens_per_req.  One kernel.
+ */
+SSD_API ssd_status_t mamba1_state_update(const mamba1_args *args, ssd_stream_t stream);
 
 #ifdef __cplusplus
 }

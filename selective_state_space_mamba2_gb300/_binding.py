@@ -22,7 +22,8 @@ DEVERR_SLOT, DEVERR_METADATA, DEVERR_COLUMN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1
 
 EXPORTED_SYMBOLS = ("ssd_status_string", "ssd_abi_version", "ssd_max_chunks", "ssd_chunk_metadata",
                     "ssd_prefill_workspace_size", "ssd_prefill_kernel_count", "ssd_prefill_varlen",
-                    "ssd_prefill_varlen_noalloc", "ssm_decode_update", "ssd_conv1d_varlen", "ssd_conv1d_update")
+                    "ssd_prefill_varlen_noalloc", "ssm_decode_update", "ssd_conv1d_varlen", "ssd_conv1d_update",
+                    "mamba1_scan_varlen", "mamba1_state_update")
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -57,6 +58,17 @@ class Conv1dArgs(ctypes.Structure):
                 ("xbc", _vp), ("weight", _vp), ("bias", _vp), ("cu_seqlens", _vp), ("cu_chunk_seqlens", _vp),
                 ("last_chunk_indices", _vp), ("init_slot", _vp), ("out_slot", _vp), ("chunk_slot", _vp),
                 ("conv_state", _vp), ("x_out", _vp), ("B_out", _vp), ("C_out", _vp), ("err_word", _vp)]
+
+
+class Mamba1Args(ctypes.Structure):
+    _fields_ = [("total_tokens", _i32), ("num_seqs", _i32), ("num_chunks", _i32), ("tokens_per_req", _i32),
+                ("dim", _i32), ("dstate", _i32), ("ngroups", _i32), ("dtype", _i32), ("dt_softplus", _i32),
+                ("dt_min", _f32), ("dt_max", _f32), ("num_slots", _i32), ("null_block_id", _i32),
+                ("state_indices_cols", _i32),
+                ("x", _vp), ("dt", _vp), ("B", _vp), ("C", _vp), ("z", _vp), ("A", _vp), ("D", _vp),
+                ("dt_bias", _vp), ("cu_seqlens", _vp), ("cu_chunk_seqlens", _vp), ("last_chunk_indices", _vp),
+                ("init_slot", _vp), ("chunk_slot", _vp), ("state_indices", _vp), ("num_accepted_tokens", _vp),
+                ("state_cache", _vp), ("y", _vp), ("err_word", _vp)]
 
 
 class SSDError(RuntimeError):
@@ -98,6 +110,9 @@ def lib():
         L.ssd_prefill_varlen_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
         L.ssm_decode_update.restype = ctypes.c_int
         L.ssm_decode_update.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        for fn in ("mamba1_scan_varlen", "mamba1_state_update"):
+            getattr(L, fn).restype = ctypes.c_int
+            getattr(L, fn).argtypes = [ctypes.POINTER(Mamba1Args), _vp]
         _lib = L
     return _lib
 
@@ -395,3 +410,84 @@ def ssd_conv1d_update(xbc, weight, conv_state, state_indices, dim_x, dim_bc, bia
     if rc != SSD_OK:
         raise SSDError("ssd_conv1d_update", rc)
     return x_out, B_out, C_out
+
+
+# ------------------------------------------------------------------ Mamba1 --
+
+def mamba1_args(x, dt, A, B, C, y, D=None, dt_bias=None, z=None, state_cache=None, dt_softplus=True,
+                dt_limit=(0.0, math.inf), null_block_id=0, err_word=None):
+    """Arguments shared by the two Mamba1 calls: x, dt, z, y [T, Dc]; B, C [T, G, N]; A [Dc, N]
+    float32; D, dt_bias [Dc] float32; state_cache [slots, Dc, N] float32."""
+    T, Dc = x.shape
+    if B.dim() != 3 or B.shape[0] != T:
+        raise ValueError("B must be [T, G, N]")
+    G, N = B.shape[1], B.shape[2]
+    for name, t, shp in (("dt", dt, (T, Dc)), ("C", C, (T, G, N)), ("y", y, (T, Dc))) + \
+            ((("z", z, (T, Dc)),) if z is not None else ()):
+        if tuple(t.shape) != shp or t.dtype != x.dtype:
+            raise ValueError("%s must be %s of shape %s" % (name, x.dtype, shp))
+    if tuple(A.shape) != (Dc, N):
+        raise ValueError("A must be [%d, %d]" % (Dc, N))
+    if state_cache is not None and tuple(state_cache.shape[1:]) != (Dc, N):
+        raise ValueError("state_cache must be [slots, %d, %d]" % (Dc, N))
+    a = Mamba1Args()
+    a.total_tokens, a.dim, a.dstate, a.ngroups = T, Dc, N, G
+    a.dtype = _dtype_code(x)
+    a.dt_softplus = int(bool(dt_softplus))
+    a.dt_min, a.dt_max = float(dt_limit[0]), float(dt_limit[1])
+    a.num_slots = 0 if state_cache is None else state_cache.shape[0]
+    a.null_block_id = int(null_block_id)
+    a.x, a.dt, a.B, a.C, a.y = _dev(x, "x"), _dev(dt, "dt"), _dev(B, "B"), _dev(C, "C"), _dev(y, "y")
+    a.z = _dev(z, "z", required=False)
+    a.A = _dev(A, "A", torch.float32)
+    a.D = _dev(D, "D", torch.float32, required=False)
+    a.dt_bias = _dev(dt_bias, "dt_bias", torch.float32, required=False)
+    a.state_cache = _dev(state_cache, "state_cache", torch.float32, required=False)
+    a.err_word = _dev(err_word, "err_word", required=False)
+    return a
+
+
+def mamba1_scan_varlen(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, last_chunk_indices, D=None, dt_bias=None,
+                       z=None, state_cache=None, init_slot=None, chunk_slot=None, dt_softplus=True,
+                       dt_limit=(0.0, math.inf), null_block_id=0, out=None, err_word=None, stream=None):
+    """Mamba1 selective scan over packed sequences; returns y [T, Dc].  Device int32 metadata
+    from ssd_chunk_metadata (chunk_size 2048 is Mamba1's default); state_cache updated in place."""
+    if out is None:
+        out = torch.empty_like(x)
+    a = mamba1_args(x, dt, A, B, C, out, D, dt_bias, z, state_cache, dt_softplus, dt_limit, null_block_id,
+                    err_word)
+    a.num_seqs = cu_seqlens.numel() - 1
+    a.num_chunks = cu_chunk_seqlens.numel() - 1
+    a.cu_seqlens = _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    a.cu_chunk_seqlens = _dev(cu_chunk_seqlens, "cu_chunk_seqlens", torch.int32)
+    a.last_chunk_indices = _dev(last_chunk_indices, "last_chunk_indices", torch.int32)
+    a.init_slot = _dev(init_slot, "init_slot", torch.int32, required=False)
+    a.chunk_slot = _dev(chunk_slot, "chunk_slot", torch.int32, required=False)
+    rc = lib().mamba1_scan_varlen(ctypes.byref(a), _stream(stream))
+    if rc != SSD_OK:
+        raise SSDError("mamba1_scan_varlen", rc)
+    return out
+
+
+def mamba1_state_update(x, dt, A, B, C, state_cache, state_indices, num_accepted_tokens=None, out=None, D=None,
+                        dt_bias=None, z=None, dt_softplus=True, dt_limit=(0.0, math.inf), null_block_id=0,
+                        err_word=None, stream=None):
+    """Mamba1 decode: in-place update of ``state_cache`` through ``state_indices`` [R, cols];
+    returns y [R * tpr, Dc]."""
+    if out is None:
+        out = torch.empty_like(x)
+    if state_indices.dim() != 2:
+        raise ValueError("state_indices must be [R, cols]")
+    R, cols = state_indices.shape
+    T = x.shape[0]
+    if R == 0 or T % R:
+        raise ValueError("x rows must be a multiple of the requests")
+    a = mamba1_args(x, dt, A, B, C, out, D, dt_bias, z, state_cache, dt_softplus, dt_limit, null_block_id,
+                    err_word)
+    a.num_seqs, a.tokens_per_req, a.state_indices_cols = R, T // R, cols
+    a.state_indices = _dev(state_indices, "state_indices", torch.int32)
+    a.num_accepted_tokens = _dev(num_accepted_tokens, "num_accepted_tokens", torch.int32, required=False)
+    rc = lib().mamba1_state_update(ctypes.byref(a), _stream(stream))
+    if rc != SSD_OK:
+        raise SSDError("mamba1_state_update", rc)
+    return out

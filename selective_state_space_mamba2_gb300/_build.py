@@ -16,7 +16,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libssd_gb300.so")
 
-SOURCES = ["api.cu", "decode.cu", "prefill_simt.cu", "prefill_tc.cu", "prefill_static.cu", "conv1d.cu", "metadata.cpp"]
+SOURCES = ["api.cu", "decode.cu", "prefill_simt.cu", "prefill_tc.cu", "prefill_static.cu", "conv1d.cu", "mamba1.cu", "metadata.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -142,3 +142,51 @@ extern "C" ssd_status_t ssd_conv1d_update(const ssd_conv1d_args *a, ssd_stream_t
     if (st != SSD_OK || a->num_seqs == 0) return st;
     return from_cuda(ssd::conv1d_launch(*a, true, reinterpret_cast<cudaStream_t>(stream)));
 }
+
+namespace {
+
+ssd_status_t check_mamba1(const mamba1_args *a, bool decode) {
+    if (!a) return SSD_ERR_INVALID_ARG;
+    if (a->total_tokens < 0 || a->num_seqs < 0 || a->num_chunks < 0) return SSD_ERR_INVALID_ARG;
+    if (a->dim <= 0 || a->ngroups <= 0 || a->dim % a->ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (!dtype_ok(a->dtype) || !limits_ok(a->dt_min, a->dt_max)) return SSD_ERR_INVALID_ARG;
+    if (a->dim % 64 != 0 || (a->dim / a->ngroups) % 64 != 0 || (a->dstate != 8 && a->dstate != 16))
+        return SSD_ERR_UNSUPPORTED;
+    if (decode) {
+        if (a->tokens_per_req < 1 || a->state_indices_cols < a->tokens_per_req ||
+            (int64_t)a->num_seqs * a->tokens_per_req != a->total_tokens)
+            return SSD_ERR_INVALID_ARG;
+    } else {
+        if (a->num_chunks > 0 && (a->total_tokens == 0 || a->num_seqs == 0)) return SSD_ERR_INVALID_ARG;
+        if (a->total_tokens > 0 && a->num_chunks == 0) return SSD_ERR_INVALID_ARG;
+    }
+    if (a->total_tokens == 0) return SSD_OK;
+    if (!a->x || !a->dt || !a->B || !a->C || !a->A || !a->y) return SSD_ERR_INVALID_ARG;
+    if (!aligned16(a->x) || !aligned16(a->dt) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->y) ||
+        (a->z && !aligned16(a->z)))
+        return SSD_ERR_INVALID_ARG;
+    if (decode) {
+        if (!a->state_indices || !a->state_cache || a->num_slots <= 0 || !aligned16(a->state_cache))
+            return SSD_ERR_INVALID_ARG;
+    } else {
+        if (!a->cu_seqlens || !a->cu_chunk_seqlens || !a->last_chunk_indices) return SSD_ERR_INVALID_ARG;
+        if ((a->init_slot || a->chunk_slot) && (!a->state_cache || a->num_slots <= 0 || !aligned16(a->state_cache)))
+            return SSD_ERR_INVALID_ARG;
+    }
+    if (a->num_seqs > 0 && (int64_t)a->dim / 64 > 65535) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" ssd_status_t mamba1_scan_varlen(const mamba1_args *a, ssd_stream_t stream) {
+    const ssd_status_t st = check_mamba1(a, false);
+    if (st != SSD_OK || a->total_tokens == 0 || a->num_seqs == 0) return st;
+    return from_cuda(ssd::mamba1_launch(*a, false, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" ssd_status_t mamba1_state_update(const mamba1_args *a, ssd_stream_t stream) {
+    const ssd_status_t st = check_mamba1(a, true);
+    if (st != SSD_OK || a->num_seqs == 0) return st;
+    return from_cuda(ssd::mamba1_launch(*a, true, reinterpret_cast<cudaStream_t>(stream)));
+}

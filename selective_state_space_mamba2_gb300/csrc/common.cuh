@@ -79,4 +79,6 @@ bool decode_supported(const ssm_decode_args &a);
 cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s);
 
 cudaError_t conv1d_launch(const ssd_conv1d_args &a, bool decode, cudaStream_t s);
+
+cudaError_t mamba1_launch(const mamba1_args &a, bool decode, cudaStream_t s);
 }  // namespace ssd

@@ -206,3 +206,40 @@ def long_mixed(device="cpu", seed=4, num_prefills=8, prefill_len=65536, num_deco
                state_indices=si, num_accepted=None, cache=cache, tokens_per_req=1,
                null_block_id=pre["null_block_id"], num_slots=num_slots, live=num_decodes)
     return pre, dec
+
+
+# Mamba1 (per-channel states): the same draws with one channel per "head" of
+# width 1, an A of shape [channels, dstate] and an optional gate z [T, channels].
+# A = -exp(U(0, ln 16)): per (channel, state index) rates spread over the range
+# of the S4D-real start values 1..16 that Mamba1 layers begin from.
+
+def mamba1_A(Dc, N, device, seed):
+    g = _gen(device, seed + 2750159)
+    return (-torch.exp(torch.rand(Dc, N, generator=g, device=device) * 2.772588722239781)).float()
+
+
+def _as_mamba1(c, N, seed, device, gate):
+    T, Dc = c["x"].shape[0], c["x"].shape[1]
+    c["x"] = c["x"].reshape(T, Dc)
+    c["cache"] = c["cache"].reshape(c["cache"].shape[0], Dc, N)
+    c["A"] = mamba1_A(Dc, N, device, seed)
+    if gate:
+        c["z"] = torch.randn(T, Dc, generator=_gen(device, seed + 3), device=device).to(c["x"].dtype)
+    return c
+
+
+def mamba1_prefill_case(seed, new_tokens, num_computed, Dc, N, G, chunk_size, dtype=torch.bfloat16, device="cpu",
+                        has_init=None, num_slots=None, null_block_id=0, gate=False):
+    """A varlen Mamba1 prefill batch ("all" cache mode): x, dt [T, Dc], B, C [T, G, N], A [Dc, N],
+    D and dt_bias [Dc], cache [slots, Dc, N] (sentinel except the slots read as initial states)."""
+    c = prefill_case(seed, new_tokens, num_computed, Dc, 1, N, G, chunk_size, dtype=dtype, device=device,
+                     has_init=has_init, num_slots=num_slots, null_block_id=null_block_id, mode="all")
+    return _as_mamba1(c, N, seed, device, gate)
+
+
+def mamba1_decode_case(seed, live, padded, tokens_per_req, Dc, N, G, num_slots, dtype=torch.bfloat16,
+                       device="cpu", null_block_id=0, gate=False):
+    """A padded Mamba1 decode batch, routed as decode_case."""
+    c = decode_case(seed, live, padded, tokens_per_req, Dc, 1, N, G, num_slots, dtype=dtype, device=device,
+                    null_block_id=null_block_id)
+    return _as_mamba1(c, N, seed, device, gate)

@@ -205,3 +205,53 @@ def test_empty_conv1d_is_a_no_op(lib):
     a = _conv_args(total_tokens=0, num_seqs=0)
     assert lib.ssd_conv1d_varlen(ctypes.byref(a), None) == B.SSD_OK
     assert lib.ssd_conv1d_update(ctypes.byref(a), None) == B.SSD_OK
+
+
+def _m1_args(**over):
+    a = B.Mamba1Args()
+    a.total_tokens, a.num_seqs, a.num_chunks, a.tokens_per_req = 8, 2, 2, 4
+    a.dim, a.dstate, a.ngroups, a.dtype, a.dt_softplus = 128, 16, 1, B.SSD_BF16, 1
+    a.dt_min, a.dt_max = 0.0, float("inf")
+    a.num_slots, a.null_block_id, a.state_indices_cols = 4, 0, 4
+    for f in ("x", "dt", "B", "C", "A", "y", "cu_seqlens", "cu_chunk_seqlens", "last_chunk_indices",
+              "state_cache", "state_indices", "init_slot"):
+        setattr(a, f, 0x10000)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dim=96), B.SSD_ERR_UNSUPPORTED),          # channels in CTAs of 64
+    (dict(dstate=4), B.SSD_ERR_UNSUPPORTED),        # dstate 8 or 16
+    (dict(ngroups=4), B.SSD_ERR_UNSUPPORTED),       # 32 channels per group: a CTA would span groups
+    (dict(ngroups=3), B.SSD_ERR_INVALID_ARG),       # groups must divide the channels
+    (dict(dtype=7), B.SSD_ERR_INVALID_ARG),
+    (dict(dt_min=2.0, dt_max=1.0), B.SSD_ERR_INVALID_ARG),
+    (dict(x=0x10008), B.SSD_ERR_INVALID_ARG),       # 16-byte copies of x rows
+    (dict(dt=0x10004), B.SSD_ERR_INVALID_ARG),
+    (dict(cu_chunk_seqlens=None), B.SSD_ERR_INVALID_ARG),
+    (dict(num_chunks=0), B.SSD_ERR_INVALID_ARG),    # tokens without chunks
+    (dict(state_cache=None), B.SSD_ERR_INVALID_ARG),  # initial-state slots without a cache
+])
+def test_mamba1_scan_host_validation(lib, over, code):
+    a = _m1_args(**over)
+    assert lib.mamba1_scan_varlen(ctypes.byref(a), None) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(tokens_per_req=3), B.SSD_ERR_INVALID_ARG),     # 2 requests x 3 tokens != 8 rows
+    (dict(state_indices_cols=3), B.SSD_ERR_INVALID_ARG),  # fewer columns than tokens per request
+    (dict(state_indices=None), B.SSD_ERR_INVALID_ARG),
+    (dict(state_cache=None), B.SSD_ERR_INVALID_ARG),
+    (dict(dstate=32), B.SSD_ERR_UNSUPPORTED),
+])
+def test_mamba1_update_host_validation(lib, over, code):
+    a = _m1_args(**over)
+    assert lib.mamba1_state_update(ctypes.byref(a), None) == code
+
+
+def test_empty_mamba1_is_a_no_op(lib):
+    a = _m1_args(total_tokens=0, num_seqs=0, num_chunks=0)
+    assert lib.mamba1_scan_varlen(ctypes.byref(a), None) == B.SSD_OK
+    assert lib.mamba1_state_update(ctypes.byref(a), None) == B.SSD_OK
