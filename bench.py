@@ -275,6 +275,67 @@ def conv1d_leg(st, steps, warmup):
             "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "kernels": 2}
 
 
+MAMBA1_SHAPE = dict(num_seqs=8, seq_len=8192, dim=5120, dstate=16, ngroups=1, chunk_size=2048, decodes=256)
+
+
+def mamba1_leg(dev, steps, warmup):
+    """The Mamba1 selective scan (a next-row step, timed on its own): 8 fresh sequences of 8192
+    tokens, 5120 channels, dstate 16, one group, bf16, states stored at every 2048-token chunk
+    end (Mamba1's default chunk); and one decode step of 256 single-token requests on a
+    [512, 5120, 16] fp32 cache.  Returns its line object."""
+    import selective_state_space_mamba2_gb300 as ssd
+    from selective_state_space_mamba2_gb300 import workloads as W
+    m = MAMBA1_SHAPE
+    S, L, Dc, N, G, Q = m["num_seqs"], m["seq_len"], m["dim"], m["dstate"], m["ngroups"], m["chunk_size"]
+    c = W.mamba1_prefill_case(4, [L] * S, [0] * S, Dc, N, G, Q, device=dev, num_slots=S * (L // Q) + 1)
+    meta = ssd.ssd_chunk_metadata(c["cu_seqlens"], Q, c["num_computed"], c["has_init"],
+                                  block_table=c["block_table"], null_block_id=0)
+    K = int(meta["cu_chunk_seqlens"].shape[0] - 1)
+    md = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in meta.items()}
+    cu = c["cu_seqlens"].to(dev)
+    y = torch.empty_like(c["x"])
+
+    def scan():
+        ssd.mamba1_scan_varlen(c["x"], c["dt"], c["A"], c["B"], c["C"], cu, md["cu_chunk_seqlens"],
+                               md["last_chunk_indices"][:S], D=c["D"], dt_bias=c["dt_bias"], state_cache=c["cache"],
+                               init_slot=md["init_slot"][:S], chunk_slot=md["chunk_slot"][:K], out=y)
+
+    R = m["decodes"]
+    dc = W.mamba1_decode_case(5, R, R, 1, Dc, N, G, 2 * R + 1, device=dev)
+    si = dc["state_indices"].to(dev)
+    yd = torch.empty_like(dc["x"])
+
+    def update():
+        ssd.mamba1_state_update(dc["x"], dc["dt"], dc["A"], dc["B"], dc["C"], dc["cache"], si, out=yd, D=dc["D"],
+                                dt_bias=dc["dt_bias"])
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms, dms = timed(scan), timed(update)
+    T = S * L
+    hbm, _ = _peaks()
+    nbytes = 3 * T * Dc * 2 + 2 * T * G * N * 2 + K * Dc * N * 4
+    dbytes = R * (2 * Dc * N * 4 + 3 * Dc * 2 + 2 * G * N * 2)
+    return {"what": "Mamba1 selective scan: %d x %d tokens, %d channels, dstate %d, bf16, states every %d tokens"
+                    % (S, L, Dc, N, Q),
+            "ms": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": nbytes,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
+            "exps_per_s": T * Dc * N / (ms * 1e-3),
+            "decode": {"requests": R, "ms": dms, "state_updates_per_s": R / (dms * 1e-3), "algorithmic_bytes": dbytes,
+                       "hbm_frac": dbytes / (dms * 1e-3) / 1e9 / hbm},
+            "kernels": 2}
+
+
 def _barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
@@ -355,6 +416,7 @@ def gpu_arm(args, rank, world, dist_on):
         e2e_value, e2e_ms = job_rate(T + R, e0.elapsed_time(e1), args.steps, dist_on, dev)
 
     conv = None if args.no_conv else conv1d_leg(st, args.steps, args.warmup)
+    m1 = None if args.no_mamba1 else mamba1_leg(dev, args.steps, args.warmup)
     if rank != 0:
         return None
     hbm, peak_kind = _peaks()
@@ -383,6 +445,7 @@ def gpu_arm(args, rank, world, dist_on):
                                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (st.prefill_kernels + (1 if R else 0)) * args.steps,
         "conv1d": conv,
+        "mamba1": m1,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -467,6 +530,7 @@ def main():
     ap.add_argument("--workload", default="long_mixed", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiler runs)")
     ap.add_argument("--no-conv", action="store_true", help="skip the conv1d measurement")
+    ap.add_argument("--no-mamba1", action="store_true", help="skip the Mamba1 measurement")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -46,28 +46,7 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 
-// N consecutive elements (16-byte aligned) -> fp32, in 16-byte loads
-template <int N>
-__device__ __forceinline__ void row_to_f32(const float *p, float (&o)[N]) {
-#pragma unroll
-    for (int i = 0; i < N / 4; ++i) {
-        const float4 v = reinterpret_cast<const float4 *>(p)[i];
-        o[4 * i] = v.x; o[4 * i + 1] = v.y; o[4 * i + 2] = v.z; o[4 * i + 3] = v.w;
-    }
-}
-template <int N>
-__device__ __forceinline__ void row_to_f32(const __nv_bfloat16 *p, float (&o)[N]) {
-#pragma unroll
-    for (int i = 0; i < N / 8; ++i) {
-        const uint4 v = reinterpret_cast<const uint4 *>(p)[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            o[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-            o[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
-    }
-}
+// N consecutive elements (16-byte aligned) of global memory -> fp32, in 16-byte loads
 template <int N, typename Tin>
 __device__ __forceinline__ void row_to_f32_ldg(const Tin *p, float (&o)[N]) {
     if constexpr (sizeof(Tin) == 4) {
@@ -90,33 +69,76 @@ __device__ __forceinline__ void row_to_f32_ldg(const Tin *p, float (&o)[N]) {
     }
 }
 
+// Packed fp32 pairs: one instruction does two lanes of work on the FMA pipe.
+__device__ __forceinline__ uint64_t pk(float2 v) { return *reinterpret_cast<uint64_t *>(&v); }
+__device__ __forceinline__ float2 upk(uint64_t v) { return *reinterpret_cast<float2 *>(&v); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
+    return upk(r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
+    return upk(r);
+}
+// 2^x on the multi-function unit; e^v is taken as 2^(v log2 e), with log2 e folded into A
+__device__ __forceinline__ float exp2_fast(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// One token of one channel: the state update and the output.  A2 = A[d, :] log2 e, so the decay
+// of state n is 2^(delta A2[n]) = exp(delta A[d, n]).
 template <int N>
-__device__ __forceinline__ void state_load(const float *p, float (&h)[N]) {
+__device__ __forceinline__ float m1_step(float2 (&h)[N / 2], const float2 (&A2)[N / 2], float delta, float xv,
+                                         const float (&Bt)[N], const float (&Ct)[N], float Dd) {
+    const float2 dd = make_float2(delta, delta);
+    const float dx = delta * xv;
+    const float2 dx2 = make_float2(dx, dx);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float2 e = mul2(dd, A2[i]);
+        const float2 a = make_float2(exp2_fast(e.x), exp2_fast(e.y));
+        h[i] = fma2(a, h[i], mul2(dx2, make_float2(Bt[2 * i], Bt[2 * i + 1])));
+        if (i & 1) acc1 = fma2(make_float2(Ct[2 * i], Ct[2 * i + 1]), h[i], acc1);
+        else acc0 = fma2(make_float2(Ct[2 * i], Ct[2 * i + 1]), h[i], acc0);
+    }
+    return fmaf(Dd, xv, (acc0.x + acc0.y) + (acc1.x + acc1.y));
+}
+
+template <typename Tin>
+__device__ __forceinline__ float m1_delta(float v, const mamba1_args &a) {
+    // bf16 tokens: the fast exp/log form (under 2e-5 relative); fp32 tokens: expf/log1pf
+    if constexpr (sizeof(Tin) == 2) return fast_delta(v, a.dt_softplus, a.dt_min, a.dt_max);
+    else return step_delta(v, a.dt_softplus, a.dt_min, a.dt_max);
+}
+
+template <int N>
+__device__ __forceinline__ void smem_row(const float *p, float (&o)[N]) {
 #pragma unroll
     for (int i = 0; i < N / 4; ++i) {
         const float4 v = reinterpret_cast<const float4 *>(p)[i];
-        h[4 * i] = v.x; h[4 * i + 1] = v.y; h[4 * i + 2] = v.z; h[4 * i + 3] = v.w;
+        o[4 * i] = v.x; o[4 * i + 1] = v.y; o[4 * i + 2] = v.z; o[4 * i + 3] = v.w;
     }
-}
-template <int N>
-__device__ __forceinline__ void state_store(float *p, const float (&h)[N]) {
-#pragma unroll
-    for (int i = 0; i < N / 4; ++i)
-        reinterpret_cast<float4 *>(p)[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
 }
 
-// One token of one channel: the state update and the output.
 template <int N>
-__device__ __forceinline__ float m1_step(float (&h)[N], const float (&Ad)[N], float delta, float xv,
-                                         const float (&Bt)[N], const float (&Ct)[N], float Dd) {
-    const float dx = delta * xv;
-    float acc = 0.f;
+__device__ __forceinline__ void state_load2(const float *p, float2 (&h)[N / 2]) {
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-        h[n] = fmaf(__expf(delta * Ad[n]), h[n], dx * Bt[n]);
-        acc = fmaf(Ct[n], h[n], acc);
+    for (int i = 0; i < N / 4; ++i) {
+        const float4 v = reinterpret_cast<const float4 *>(p)[i];
+        h[2 * i] = make_float2(v.x, v.y);
+        h[2 * i + 1] = make_float2(v.z, v.w);
     }
-    return fmaf(Dd, xv, acc);
+}
+template <int N>
+__device__ __forceinline__ void state_store2(float *p, const float2 (&h)[N / 2]) {
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i)
+        reinterpret_cast<float4 *>(p)[i] = make_float4(h[2 * i].x, h[2 * i].y, h[2 * i + 1].x, h[2 * i + 1].y);
 }
 
 // Tiles of at most kTc tokens of one sequence, never crossing a chunk end.
@@ -150,7 +172,9 @@ __global__ void __launch_bounds__(kCh) mamba1_scan_kernel(const mamba1_args a) {
     constexpr int kTileX = kTc * kRow;
     constexpr int kTileBC = kTc * kBc;
     constexpr int kStage = (kGate ? 3 : 2) * kTileX + 2 * kTileBC;
+    constexpr bool kConvert = sizeof(Tin) != 4;  // bf16 B/C rows are widened to fp32 once per tile
     __shared__ __align__(16) uint8_t sm[2 * kStage];
+    __shared__ __align__(16) float sBCf[kConvert ? 2 * kTc * N : 4];
 
     const int r = blockIdx.x, tid = threadIdx.x;
     const int Dc = a.dim, G = a.ngroups;
@@ -176,16 +200,18 @@ __global__ void __launch_bounds__(kCh) mamba1_scan_kernel(const mamba1_args a) {
         }
     }
 
-    float h[N], Ad[N];
+    constexpr float kLog2e = 1.4426950408889634f;
+    float2 h[N / 2], A2[N / 2];
     {
         const int32_t is = a.init_slot ? a.init_slot[r] : a.null_block_id;
         if (slot_usable(is, a.null_block_id, a.num_slots, (tid == 0) ? a.err_word : nullptr))
-            state_load<N>(a.state_cache + ((size_t)is * Dc + d) * N, h);
+            state_load2<N>(a.state_cache + ((size_t)is * Dc + d) * N, h);
         else
 #pragma unroll
-            for (int n = 0; n < N; ++n) h[n] = 0.f;
+            for (int i = 0; i < N / 2; ++i) h[i] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int n = 0; n < N; ++n) Ad[n] = a.A[(size_t)d * N + n];
+        for (int i = 0; i < N / 2; ++i)
+            A2[i] = make_float2(a.A[(size_t)d * N + 2 * i] * kLog2e, a.A[(size_t)d * N + 2 * i + 1] * kLog2e);
     }
     const float Dd = a.D ? a.D[d] : 0.f;
     const float bias = a.dt_bias ? a.dt_bias[d] : 0.f;
@@ -236,26 +262,65 @@ __global__ void __launch_bounds__(kCh) mamba1_scan_kernel(const mamba1_args a) {
         const Tin *dts = reinterpret_cast<const Tin *>(st + kTileX);
         const Tin *zs = reinterpret_cast<const Tin *>(st + 2 * kTileX);
         const uint8_t *sb = st + (kGate ? 3 : 2) * kTileX;
-        const Tin *Bs = reinterpret_cast<const Tin *>(sb);
-        const Tin *Cs = reinterpret_cast<const Tin *>(sb + kTileBC);
         const int tb = cur.tb, L = cur.len();
-        for (int t = 0; t < L; ++t) {
-            float Bt[N], Ct[N];
-            row_to_f32<N>(Bs + t * N, Bt);
-            row_to_f32<N>(Cs + t * N, Ct);
-            const float xv = to_f32(xs[t * kCh + tid]);
-            const float delta = step_delta(to_f32(dts[t * kCh + tid]) + bias, a.dt_softplus, a.dt_min, a.dt_max);
-            float yv = m1_step<N>(h, Ad, delta, xv, Bt, Ct, Dd);
-            if (kGate) yv = silu_gate(yv, to_f32(zs[t * kCh + tid]));
-            y[(size_t)(tb + t) * Dc + d] = from_f32<Tin>(yv);
+        const float *Bf, *Cf;  // the tile's B and C rows in fp32, [kTc][N] each
+        if constexpr (kConvert) {
+            const uint4 *raw = reinterpret_cast<const uint4 *>(sb);  // B rows then C rows, 8 bf16 per uint4
+            for (int i = tid; i < 2 * L * N / 8; i += kCh) {
+                const int which = i / (L * N / 8), j = i - which * (L * N / 8);
+                const uint4 v = raw[which * (kTc * N / 8) + j];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                float4 *o = reinterpret_cast<float4 *>(sBCf + which * kTc * N + 8 * j);
+                o[0] = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
+                                   __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
+                o[1] = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
+                                   __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
+            }
+            __syncthreads();
+            Bf = sBCf;
+            Cf = sBCf + kTc * N;
+        } else {
+            Bf = reinterpret_cast<const float *>(sb);
+            Cf = reinterpret_cast<const float *>(sb + kTileBC);
+        }
+        // two tokens per step: the second token's loads, delta and decays do not depend on the
+        // first token's state, so they overlap its update
+        int t = 0;
+        for (; t + 2 <= L; t += 2) {
+            float B0[N], C0[N], B1[N], C1[N];
+            smem_row<N>(Bf + t * N, B0);
+            smem_row<N>(Cf + t * N, C0);
+            smem_row<N>(Bf + (t + 1) * N, B1);
+            smem_row<N>(Cf + (t + 1) * N, C1);
+            const float x0 = to_f32(xs[t * kCh + tid]), x1 = to_f32(xs[(t + 1) * kCh + tid]);
+            const float dl0 = m1_delta<Tin>(to_f32(dts[t * kCh + tid]) + bias, a);
+            const float dl1 = m1_delta<Tin>(to_f32(dts[(t + 1) * kCh + tid]) + bias, a);
+            float y0 = m1_step<N>(h, A2, dl0, x0, B0, C0, Dd);
+            float y1 = m1_step<N>(h, A2, dl1, x1, B1, C1, Dd);
+            if (kGate) {
+                y0 = silu_gate(y0, to_f32(zs[t * kCh + tid]));
+                y1 = silu_gate(y1, to_f32(zs[(t + 1) * kCh + tid]));
+            }
+            y[(size_t)(tb + t) * Dc + d] = from_f32<Tin>(y0);
+            y[(size_t)(tb + t + 1) * Dc + d] = from_f32<Tin>(y1);
+        }
+        if (t < L) {
+            float B0[N], C0[N];
+            smem_row<N>(Bf + t * N, B0);
+            smem_row<N>(Cf + t * N, C0);
+            const float x0 = to_f32(xs[t * kCh + tid]);
+            const float dl0 = m1_delta<Tin>(to_f32(dts[t * kCh + tid]) + bias, a);
+            float y0 = m1_step<N>(h, A2, dl0, x0, B0, C0, Dd);
+            if (kGate) y0 = silu_gate(y0, to_f32(zs[t * kCh + tid]));
+            y[(size_t)(tb + t) * Dc + d] = from_f32<Tin>(y0);
         }
         if (cur.ends_chunk()) {
             if (slot_usable(cs, a.null_block_id, a.num_slots, (tid == 0) ? a.err_word : nullptr))
-                state_store<N>(a.state_cache + ((size_t)cs * Dc + d) * N, h);
+                state_store2<N>(a.state_cache + ((size_t)cs * Dc + d) * N, h);
             if (a.chunk_slot) cs = a.chunk_slot[min(cur.k + 1, last)];
         }
         cur.next();
-        __syncthreads();  // every thread is done with buffer (i & 1) before it is refilled
+        __syncthreads();  // every thread is done with buffer (i & 1) and the fp32 rows before reuse
     }
 }
 
@@ -278,10 +343,12 @@ __global__ void __launch_bounds__(kCh) mamba1_update_kernel(const mamba1_args a)
         if (tid == 0 && blockIdx.y == 0) report(a.err_word, SSD_DEVERR_SLOT);
         return;
     }
-    float h[N], Ad[N];
-    state_load<N>(a.state_cache + ((size_t)rs * Dc + d) * N, h);
+    constexpr float kLog2e = 1.4426950408889634f;
+    float2 h[N / 2], A2[N / 2];
+    state_load2<N>(a.state_cache + ((size_t)rs * Dc + d) * N, h);
 #pragma unroll
-    for (int n = 0; n < N; ++n) Ad[n] = a.A[(size_t)d * N + n];
+    for (int i = 0; i < N / 2; ++i)
+        A2[i] = make_float2(a.A[(size_t)d * N + 2 * i] * kLog2e, a.A[(size_t)d * N + 2 * i + 1] * kLog2e);
     const float Dd = a.D ? a.D[d] : 0.f;
     const float bias = a.dt_bias ? a.dt_bias[d] : 0.f;
     const Tin *x = static_cast<const Tin *>(a.x), *dt = static_cast<const Tin *>(a.dt);
@@ -294,13 +361,13 @@ __global__ void __launch_bounds__(kCh) mamba1_update_kernel(const mamba1_args a)
         row_to_f32_ldg<N>(Bp + (row * G + g) * N, Bt);
         row_to_f32_ldg<N>(Cp + (row * G + g) * N, Ct);
         const float xv = ldg_f32(x + row * Dc + d);
-        const float delta = step_delta(ldg_f32(dt + row * Dc + d) + bias, a.dt_softplus, a.dt_min, a.dt_max);
-        float yv = m1_step<N>(h, Ad, delta, xv, Bt, Ct, Dd);
+        const float delta = m1_delta<Tin>(ldg_f32(dt + row * Dc + d) + bias, a);
+        float yv = m1_step<N>(h, A2, delta, xv, Bt, Ct, Dd);
         if (kGate) yv = silu_gate(yv, ldg_f32(z + row * Dc + d));
         y[row * Dc + d] = from_f32<Tin>(yv);
         const int32_t ws = row_slots[k];
         if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr))
-            state_store<N>(a.state_cache + ((size_t)ws * Dc + d) * N, h);
+            state_store2<N>(a.state_cache + ((size_t)ws * Dc + d) * N, h);
     }
 }
 

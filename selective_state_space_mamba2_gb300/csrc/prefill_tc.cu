@@ -135,20 +135,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     return ok;
 }
 
-// delta = clamp(softplus(v), lo, hi) from the fast exp/log intrinsics:
-// softplus(v) = v above 15 (the rest is below e^-15 relative); e - e^2/2 with
-// e = exp(v) below -5 (log1p's series; the next term is under 2e-5
-// relative there); log(1 + e) in between, where 1 + e >= 1.0067 keeps the
-// rounding of the sum under 1e-5 relative.
-__device__ __forceinline__ float fast_delta(float v, int dt_softplus, float lo, float hi) {
-    float d = v;
-    if (dt_softplus && v <= 15.f) {
-        const float e = __expf(v);
-        d = v < -5.f ? e * (1.f - 0.5f * e) : __logf(1.f + e);
-    }
-    return fminf(fmaxf(d, lo), hi);
-}
-
 // Walks the blocks of one sequence: chunks [first, last], each cut into
 // blocks of at most kL tokens that never cross a chunk end.  The end of the
 // following chunk is loaded one chunk ahead (from a clamped index, so the
