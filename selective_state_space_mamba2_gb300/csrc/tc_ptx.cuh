@@ -110,6 +110,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, int
         : "memory");
 }
 
+// 2-D tiled load into shared memory, completion counted on `bar` (bytes).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM ------
 // Warp-wide: allocates `ncols` (power of two >= 32) TMEM columns and writes
 // the base address to *dst_smem.

@@ -38,6 +38,22 @@ inline bool make_tmap_16bit_3d(CUtensorMap *m, CUtensorMapDataType type, const v
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major 2-D tensor [rows, cols] of 2- or 4-byte elements (cols innermost, row stride in
+// bytes), box (box_cols, box_rows), no swizzle: the box lands in shared memory as box_rows
+// rows of box_cols elements.  Elements outside the tensor read as zeros.
+inline bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t cols, uint64_t rows,
+                         uint64_t row_stride, uint32_t box_cols, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_stride};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline bool make_tmap_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
                               uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
     return make_tmap_16bit_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d0, d1, d2, s1, s2, b0, b1, b2);
