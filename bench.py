@@ -64,10 +64,10 @@ def _peaks():
 # ------------------------------------------------------------- byte counts --
 
 # DRAM traffic of one prefill call, from one ncu capture of the fused kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum = 3.472 GB for 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256), scaled
+# dram__bytes_write.sum = 3.471 GB for 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256), scaled
 # by tokens (x, y, B/C and one state per chunk all grow with them), plus the B/C pre-conversion, which
 # streams 2*T*G*N*2 bytes in and as many out.  Only for that head configuration and kernel version.
-FUSED_TRAFFIC_PER_TOKEN = 3.472e9 / 65536
+FUSED_TRAFFIC_PER_TOKEN = 3.471e9 / 65536
 
 
 def prefill_traffic(T, H, P, N, G):
