@@ -178,7 +178,12 @@ class Step:
                              p["cache"], p["D"], p["dt_bias"], chunk_size=p["chunk_size"], seq_order=m["seq_order"])
         self.workspace = torch.empty(max(ssd.ssd_prefill_workspace_size(a), 1), dtype=torch.uint8, device=dev)
         self.prefill_kernels = ssd.ssd_prefill_kernel_count(a)
-        self.stream = torch.cuda.current_stream()
+        # The mixed step runs the prefill on a high-priority stream and the decode on a
+        # normal-priority one.  A prefill CTA needs a whole SM (shared memory, TMEM), so pending
+        # prefill CTAs take every SM that frees up first; decode CTAs fill the SMs the prefill's
+        # last, partial wave leaves idle.
+        self.hi = torch.cuda.Stream(device=dev, priority=-5)
+        self.side = torch.cuda.Stream(device=dev, priority=0)
 
     def metadata(self):
         p = self.pre
@@ -188,16 +193,22 @@ class Step:
     def device_meta(self, meta):
         return {k: torch.from_numpy(v).to(self.dev, non_blocking=True) for k, v in meta.items()}
 
-    def run(self, ev=None, host=None):
-        """One step.  ev: optional (start, mid, end) CUDA events around the
-        prefill and decode calls.  host: pinned host buffers for the e2e leg."""
+    def run(self, ev=None, host=None, mixed=False):
+        """One step on the current stream.  ev: optional (start, mid, end) CUDA events around
+        the prefill and decode calls (serial step only).  host: pinned host buffers for the e2e
+        leg.  mixed: the decode runs on the side stream beside the prefill (see __init__)."""
         p, d = self.pre, self.dec
+        main = torch.cuda.current_stream()
         if host is not None:  # end to end: this step's inputs come from host memory
             for name in ("x", "dt", "B", "C"):
                 p[name].copy_(host["p_" + name], non_blocking=True)
                 d[name].copy_(host["d_" + name], non_blocking=True)
         meta = self.metadata()
         m = self.device_meta(meta)
+        ready = None
+        if mixed:
+            ready = torch.cuda.Event()
+            ready.record(main)  # inputs and metadata are in place
         if ev is not None:
             ev[0].record()
         self.ssd.ssd_prefill_varlen(p["x"], p["dt"], p["A"], p["B"], p["C"], self.cu_dev, m["cu_chunk_seqlens"],
@@ -208,9 +219,17 @@ class Step:
         if ev is not None:
             ev[1].record()
         if self.dec["live"] > 0:
-            self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
-                                       out=self.yd, D=d["D"], dt_bias=d["dt_bias"],
-                                       null_block_id=d["null_block_id"])
+            if mixed:
+                self.side.wait_event(ready)
+                with torch.cuda.stream(self.side):
+                    self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
+                                               out=self.yd, D=d["D"], dt_bias=d["dt_bias"],
+                                               null_block_id=d["null_block_id"])
+                main.wait_stream(self.side)
+            else:
+                self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
+                                           out=self.yd, D=d["D"], dt_bias=d["dt_bias"],
+                                           null_block_id=d["null_block_id"])
         if ev is not None:
             ev[2].record()
         if host is not None:
@@ -379,7 +398,10 @@ def gpu_arm(args, rank, world, dist_on):
     R = st.dec["live"]
     pre_bytes = prefill_bytes(T, st.K, H, P, N, G, 2)
     dec_bytes = decode_bytes(R, 1, R, H, P, N, G, 2)
+    mixed = not args.serial_step
+    torch.cuda.set_stream(st.hi)  # every timed step is issued on the high-priority stream
     for _ in range(args.warmup):
+        st.run(mixed=mixed)
         st.run()
     torch.cuda.synchronize()
 
@@ -387,15 +409,20 @@ def gpu_arm(args, rank, world, dist_on):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
+        # the step: prefill and decode together (the headline)
         _barrier(dist_on)
         torch.cuda.synchronize()
         t0.record()
         for i in range(args.steps):
-            st.run(ev=evs[i])
+            st.run(mixed=mixed)
         t1.record()
         torch.cuda.synchronize()
         _barrier(dist_on)
-    value, ms_step = job_rate(T + R, t0.elapsed_time(t1), args.steps, dist_on, dev)
+        value, ms_step = job_rate(T + R, t0.elapsed_time(t1), args.steps, dist_on, dev)
+        # each call on its own (per-call times, the roofline)
+        for i in range(args.steps):
+            st.run(ev=evs[i])
+        torch.cuda.synchronize()
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
 
@@ -403,14 +430,14 @@ def gpu_arm(args, rank, world, dist_on):
     e2e_value, e2e_ms, h2d, d2h = None, None, 0, 0
     if not args.no_e2e:
         host, h2d, d2h = st.host_buffers()
-        st.run(host=host)
+        st.run(host=host, mixed=mixed)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         _barrier(dist_on)
         e0.record()
         for _ in range(args.steps):
-            st.run(host=host)
+            st.run(host=host, mixed=mixed)
         e1.record()
         torch.cuda.synchronize()
         e2e_value, e2e_ms = job_rate(T + R, e0.elapsed_time(e1), args.steps, dist_on, dev)
@@ -428,7 +455,9 @@ def gpu_arm(args, rank, world, dist_on):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded randn tokens, -exp(U(0,2)) A, U(-4,-1) dt_bias)",
-        "config": dict(wl, parallelism="dp%d (independent replicas)" % world),
+        "config": dict(wl, parallelism="dp%d (independent replicas)" % world,
+                       step="prefill on a high-priority stream, decode beside it on a normal-priority one"
+                       if mixed else "prefill then decode on one stream"),
         "prefill": {"tokens_per_s_per_layer": T / (pre_mean * 1e-3), "ms": pre_mean,
                     "algorithmic_bytes": pre_bytes,
                     "hbm_frac": achieved / hbm},
@@ -531,6 +560,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiler runs)")
     ap.add_argument("--no-conv", action="store_true", help="skip the conv1d measurement")
     ap.add_argument("--no-mamba1", action="store_true", help="skip the Mamba1 measurement")
+    ap.add_argument("--serial-step", action="store_true", help="run the step's decode after the prefill on one stream")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
