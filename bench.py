@@ -453,9 +453,34 @@ def job_rate(local_units, local_ms, steps, dist_on, dev):
     return units / (ms / steps * 1e-3), ms / steps
 
 
+def _bind_to_gpu_numa(dev):
+    """Run this process on the CPUs of the GPU's own NUMA node, so the pinned host buffers of
+    the e2e leg (allocated by this thread) sit next to the GPU's host link.  Returns the node,
+    or None where the system does not say."""
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bdf = "%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/numa_node" % bdf) as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return None
+        with open("/sys/devices/system/node/node%d/cpulist" % node) as f:
+            cpus = set()
+            for part in f.read().strip().split(","):
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+            return node
+    except (OSError, ValueError, AttributeError):
+        pass
+    return None
+
+
 def gpu_arm(args, rank, world, dist_on):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    numa = _bind_to_gpu_numa(dev)
     import selective_state_space_mamba2_gb300 as ssd
     ssd.build()
     wl = WORKLOADS[args.workload]
@@ -516,7 +541,7 @@ def gpu_arm(args, rank, world, dist_on):
         "data": "synthetic (seeded randn tokens, -exp(U(0,2)) A, U(-4,-1) dt_bias)",
         "config": dict(wl, parallelism="dp%d (independent replicas)" % world,
                        step="prefill on a high-priority stream, decode beside it on a normal-priority one"
-                       if mixed else "prefill then decode on one stream"),
+                       if mixed else "prefill then decode on one stream", host_numa_node=numa),
         "prefill": {"tokens_per_s_per_layer": T / (pre_mean * 1e-3), "ms": pre_mean,
                     "algorithmic_bytes": pre_bytes,
                     "hbm_frac": achieved / hbm},
