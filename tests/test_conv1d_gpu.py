@@ -53,7 +53,7 @@ def _mark_unused(state, used):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("W", [4, 2])
+@pytest.mark.parametrize("W", [4, 3, 2])
 def test_conv1d_varlen_prefix_cached(dtype, W):
     """Ragged packed sequences with unaligned computed prefixes (partial first
     chunks), an empty sequence, sequences shorter than W - 1, mixed initial
