@@ -362,6 +362,10 @@ def conv1d_leg(st, steps, warmup):
 
 
 MAMBA1_SHAPE = dict(num_seqs=8, seq_len=8192, dim=5120, dstate=16, ngroups=1, chunk_size=2048, decodes=256)
+# The Mamba1 scan is bound by the multi-function unit (one base-2 exponential per token, channel and
+# state): 16 results per clock per SM, at the GB300's maximum SM clock.
+MUFU_EX2_PER_SM_CLOCK = 16
+SM_MAX_MHZ = 2070.0
 
 
 def mamba1_leg(dev, steps, warmup):
@@ -410,6 +414,8 @@ def mamba1_leg(dev, steps, warmup):
     ms, dms = timed(scan), timed(update)
     T = S * L
     hbm, _ = _peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mufu_peak = sms * MUFU_EX2_PER_SM_CLOCK * SM_MAX_MHZ * 1e6 / 1e12
     nbytes = 3 * T * Dc * 2 + 2 * T * G * N * 2 + K * Dc * N * 4
     dbytes = R * (2 * Dc * N * 4 + 3 * Dc * 2 + 2 * G * N * 2)
     return {"what": "Mamba1 selective scan: %d x %d tokens, %d channels, dstate %d, bf16, states every %d tokens"
@@ -417,6 +423,10 @@ def mamba1_leg(dev, steps, warmup):
             "ms": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": nbytes,
             "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
             "exps_per_s": T * Dc * N / (ms * 1e-3),
+            "roofline": {"bound": "alu", "achieved": T * Dc * N / (ms * 1e-3) / 1e12, "peak": mufu_peak,
+                         "unit": "Tex2/s", "frac": T * Dc * N / (ms * 1e-3) / 1e12 / mufu_peak,
+                         "peak_source": "derived: %d SMs x %d ex2 per clock x %.0f MHz"
+                                        % (sms, MUFU_EX2_PER_SM_CLOCK, SM_MAX_MHZ)},
             "decode": {"requests": R, "ms": dms, "state_updates_per_s": R / (dms * 1e-3), "algorithmic_bytes": dbytes,
                        "hbm_frac": dbytes / (dms * 1e-3) / 1e9 / hbm},
             "kernels": 2}
