@@ -61,6 +61,24 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _bf16_peak():
+    """Dense bf16 tensor TFLOP/s for a kernel timed on its own (the burst figure); fp16 operands
+    run at the same rate."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def _sm_max_mhz():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        return SM_MAX_MHZ
+
+
 # ------------------------------------------------------------- byte counts --
 
 # DRAM traffic of one prefill call, from one ncu capture of the fused kernel (dram__bytes_read.sum +
@@ -68,6 +86,7 @@ def _peaks():
 # by tokens (x, y, B/C and one state per chunk all grow with them), plus the B/C pre-conversion, which
 # streams 2*T*G*N*2 bytes in and as many out.  Only for that head configuration and kernel version.
 FUSED_TRAFFIC_PER_TOKEN = 3.471e9 / 65536
+SM_MAX_MHZ = 2070.0  # GB300's maximum SM clock, where the measured-peaks file does not give it
 
 
 def prefill_traffic(T, H, P, N, G):
@@ -81,6 +100,21 @@ def prefill_bytes(T, K, H, P, N, G, elt, init_reads=0):
     token; one fp32 state store per chunk; one state load per initial state."""
     per_tok = 2 * H * P * elt + H * elt + 2 * G * N * elt
     return T * per_tok + (K + init_reads) * H * P * N * 4
+
+
+# The fused prefill cuts every chunk into blocks of at most 128 tokens and issues, per block and
+# head, four dense products on full 128-row tiles: S = C B^T (128 x 128, K = N), Y1 = P X
+# (128 x P, K = 128), Y2 = C Hprev^T (128 x P, K = N) and dS = B^T (w x) (N x P, K = 128).
+TC_BLOCK = 128
+
+
+def prefill_mma_flops(cu_chunk_seqlens, H, P, N):
+    """Tensor-core flops one fused prefill call issues (the masked upper half of S and P included)."""
+    lens = np.diff(np.asarray(cu_chunk_seqlens, dtype=np.int64))
+    blocks = int(((lens + TC_BLOCK - 1) // TC_BLOCK).sum())
+    L = TC_BLOCK
+    per_block_head = 2 * (L * L * N + L * P * L + L * P * N + N * P * L)
+    return blocks * H * per_block_head
 
 
 def decode_bytes(live, tpr, writes, H, P, N, G, elt):
@@ -365,7 +399,6 @@ MAMBA1_SHAPE = dict(num_seqs=8, seq_len=8192, dim=5120, dstate=16, ngroups=1, ch
 # The Mamba1 scan is bound by the multi-function unit (one base-2 exponential per token, channel and
 # state): 16 results per clock per SM, at the GB300's maximum SM clock.
 MUFU_EX2_PER_SM_CLOCK = 16
-SM_MAX_MHZ = 2070.0
 
 
 def mamba1_leg(dev, steps, warmup):
@@ -415,7 +448,8 @@ def mamba1_leg(dev, steps, warmup):
     T = S * L
     hbm, _ = _peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    mufu_peak = sms * MUFU_EX2_PER_SM_CLOCK * SM_MAX_MHZ * 1e6 / 1e12
+    mhz = _sm_max_mhz()
+    mufu_peak = sms * MUFU_EX2_PER_SM_CLOCK * mhz * 1e6 / 1e12
     nbytes = 3 * T * Dc * 2 + 2 * T * G * N * 2 + K * Dc * N * 4
     dbytes = R * (2 * Dc * N * 4 + 3 * Dc * 2 + 2 * G * N * 2)
     return {"what": "Mamba1 selective scan: %d x %d tokens, %d channels, dstate %d, bf16, states every %d tokens"
@@ -426,7 +460,7 @@ def mamba1_leg(dev, steps, warmup):
             "roofline": {"bound": "alu", "achieved": T * Dc * N / (ms * 1e-3) / 1e12, "peak": mufu_peak,
                          "unit": "Tex2/s", "frac": T * Dc * N / (ms * 1e-3) / 1e12 / mufu_peak,
                          "peak_source": "derived: %d SMs x %d ex2 per clock x %.0f MHz"
-                                        % (sms, MUFU_EX2_PER_SM_CLOCK, SM_MAX_MHZ)},
+                                        % (sms, MUFU_EX2_PER_SM_CLOCK, mhz)},
             "decode": {"requests": R, "ms": dms, "state_updates_per_s": R / (dms * 1e-3), "algorithmic_bytes": dbytes,
                        "hbm_frac": dbytes / (dms * 1e-3) / 1e9 / hbm},
             "kernels": 2}
@@ -541,6 +575,8 @@ def gpu_arm(args, rank, world, dist_on):
     if rank != 0:
         return None
     hbm, peak_kind = _peaks()
+    bf16, bf16_kind = _bf16_peak()
+    pre_flops = prefill_mma_flops(st.meta["cu_chunk_seqlens"], H, P, N)
     pre_mean = statistics.mean(pre_ms)
     dec_mean = statistics.mean(dec_ms) if R > 0 else 0.0
     achieved = pre_bytes / (pre_mean * 1e-3) / 1e9
@@ -554,7 +590,12 @@ def gpu_arm(args, rank, world, dist_on):
                        if mixed else "prefill then decode on one stream", host_numa_node=numa),
         "prefill": {"tokens_per_s_per_layer": T / (pre_mean * 1e-3), "ms": pre_mean,
                     "algorithmic_bytes": pre_bytes,
-                    "hbm_frac": achieved / hbm},
+                    "hbm_frac": achieved / hbm,
+                    "tensor": {"achieved": pre_flops / (pre_mean * 1e-3) / 1e12, "peak": bf16,
+                               "unit": "TFLOP/s", "frac": pre_flops / (pre_mean * 1e-3) / 1e12 / bf16,
+                               "flops": pre_flops, "peak_source": bf16_kind,
+                               "what": "tcgen05 flops the fused kernel issues: four products per 128-token "
+                                       "block and head on full tiles, fp16 operands, fp32 accumulators"}},
         "decode": {"state_updates_per_s": R / (dec_mean * 1e-3) if R else None, "ms": dec_mean,
                    "algorithmic_bytes": dec_bytes,
                    "hbm_frac": dec_bytes / (dec_mean * 1e-3) / 1e9 / hbm if R else None},
