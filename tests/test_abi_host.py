@@ -127,6 +127,28 @@ def test_prefill_workspace_too_small_is_refused(lib):
     assert lib.ssd_prefill_varlen(ctypes.byref(a), ctypes.c_void_p(0x100010), need, None) == B.SSD_ERR_WORKSPACE
 
 
+def _up256(n):
+    return (n + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("T,H,K,P,N", [(8, 2, 1, 4, 4), (2048, 48, 1, 64, 128), (3, 1, 3, 8, 16), (1000, 48, 5, 64, 128)])
+def test_cuda_core_workspace_is_the_documented_formula(lib, T, H, K, P, N):
+    """ssd.h gives the CUDA-core path's scratch as up256(4HT) + up256(8HT) + 2 up256(4KHPN);
+    one 2048-token chunk at H=48, P=64, N=128 is its "about 4.3 MB" example."""
+    a = _prefill_args(total_tokens=T, nheads=H, num_chunks=K, headdim=P, dstate=N)
+    need = lib.ssd_prefill_workspace_size(ctypes.byref(a))
+    assert need == _up256(4 * H * T) + _up256(8 * H * T) + 2 * _up256(4 * K * H * P * N)
+    if (T, H, K) == (2048, 48, 1):
+        assert round(need / 1e6, 1) == 4.3
+
+
+def test_noalloc_refusal_is_decided_on_the_host(lib):
+    # 40 chunks of states at H=48, P=64, N=128 need 2 * 40 * 1.57 MB of scratch, beyond 64 MiB
+    a = _prefill_args(total_tokens=2048, num_chunks=40, nheads=48, headdim=64, dstate=128)
+    assert lib.ssd_prefill_workspace_size(ctypes.byref(a)) > 64 << 20
+    assert lib.ssd_prefill_varlen_noalloc(ctypes.byref(a), None) == B.SSD_ERR_WORKSPACE
+
+
 def test_empty_prefill_is_a_no_op(lib):
     a = _prefill_args(total_tokens=0, num_chunks=0)
     assert lib.ssd_prefill_varlen(ctypes.byref(a), None, 0, None) == B.SSD_OK
