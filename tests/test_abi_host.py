@@ -142,6 +142,14 @@ def test_cuda_core_workspace_is_the_documented_formula(lib, T, H, K, P, N):
         assert round(need / 1e6, 1) == 4.3
 
 
+@pytest.mark.parametrize("T,G", [(1, 1), (777, 8), (65536, 8)])
+def test_tensor_core_workspace_is_the_documented_formula(lib, T, G):
+    """bf16 with headdim 64 and dstate 128: fp16 copies of B and C, 2 up256(2 T G N) bytes."""
+    a = _prefill_args(total_tokens=T, nheads=2 * G, ngroups=G, headdim=64, dstate=128, dtype=B.SSD_BF16)
+    assert lib.ssd_prefill_kernel_count(ctypes.byref(a)) == 2
+    assert lib.ssd_prefill_workspace_size(ctypes.byref(a)) == 2 * _up256(2 * T * G * 128)
+
+
 def test_noalloc_refusal_is_decided_on_the_host(lib):
     # 40 chunks of states at H=48, P=64, N=128 need 2 * 40 * 1.57 MB of scratch, beyond 64 MiB
     a = _prefill_args(total_tokens=2048, num_chunks=40, nheads=48, headdim=64, dstate=128)
