@@ -51,3 +51,23 @@ def test_peaks_come_from_the_measured_file_when_present():
         assert bench._sm_max_mhz() == float(m["sm_max_mhz"])
     else:
         assert kind == "fallback" and bkind == "fallback"
+
+
+def test_reference_arm_prints_one_json_line():
+    """`bench.py --impl reference` (the oracle on the host cores) needs no GPU: one JSON line with
+    the native arm's metric and unit, impl "reference", its cpu_baseline and a host-only e2e."""
+    import json
+    import subprocess
+    root = bench.ROOT
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["steps"] == 1 and d["higher_is_better"] is True
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"]
