@@ -285,3 +285,34 @@ def test_empty_mamba1_is_a_no_op(lib):
     a = _m1_args(total_tokens=0, num_seqs=0, num_chunks=0)
     assert lib.mamba1_scan_varlen(ctypes.byref(a), None) == B.SSD_OK
     assert lib.mamba1_state_update(ctypes.byref(a), None) == B.SSD_OK
+
+
+def test_calls_fail_loudly_without_the_library(monkeypatch, tmp_path):
+    """There is no implementation behind the binding but the CUDA library: without it every call
+    raises instead of computing anything."""
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        ssd.ssd_max_chunks(1, 8, 4)
+    with pytest.raises(RuntimeError, match="missing"):
+        ssd.ssd_chunk_metadata([0, 5], 4)
+    with pytest.raises(RuntimeError, match="missing"):
+        B.lib()
+
+
+def test_device_calls_refuse_host_tensors():
+    """Host (CPU) tensors are refused by every device call: there is no CPU path to fall back to."""
+    import torch
+    R, H, P, N = 2, 2, 4, 8
+    x = torch.zeros(R, H, P, dtype=torch.bfloat16)
+    dt = torch.zeros(R, H, dtype=torch.bfloat16)
+    Bm = torch.zeros(R, 1, N, dtype=torch.bfloat16)
+    A = torch.full((H,), -1.0)
+    cache = torch.zeros(4, H, P, N)
+    si = torch.ones(R, 1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ssd.ssm_decode_update(x, dt, A, Bm, Bm, cache, si)
+    cu = torch.tensor([0, R], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ssd.ssd_prefill_varlen(x, dt, A, Bm, Bm, cu, cu, torch.zeros(1, dtype=torch.int32),
+                               torch.zeros(1, dtype=torch.int32))
