@@ -156,3 +156,38 @@ def test_mamba1_prefill_then_decode_equals_longer_prefill(oracle_lib, null):
     assert F.rel_err(new[4], fs_full[0]) < 1e-13
     keep = [i for i in range(6) if i not in (2, 4)]
     assert np.array_equal(new[keep], cache[keep])
+
+
+@pytest.mark.parametrize("null", [0, -1])
+def test_mamba1_cache_routing_hand_written(oracle_lib, null):
+    """Slot routing of the Mamba1 state cache on hand-written slot lists
+    ("[vLLM] Mamba (SSM) ...", "청크 메타데이터 계산": the state is taken out at
+    every chunk end): sequence 0 resumes from slot 2, which its first chunk
+    then overwrites (read before write); sequence 1 has a null initial slot
+    (zero state); one chunk slot is null.  Expected values come from the
+    independent matrix form, each segment started from the state the slot
+    list names; slots no chunk writes keep their bits."""
+    rng = np.random.default_rng(8)
+    Dc, N, G = 4, 3, 1
+    cu = [0, 13, 20]
+    cc = [0, 5, 13, 16, 20]
+    x, dt, A, B, C, D, dt_bias = _case(rng, 20, Dc, N, G)
+    cache = rng.standard_normal((8, Dc, N))
+    init_slot = [2, null]
+    chunk_slot = [2, 5, null, 6]
+    y, new = oracle_lib.mamba1_prefill_with_cache(x, dt, A, B, C, cu, cc, init_slot, chunk_slot, null,
+                                                  cache, D=D, dt_bias=dt_bias)
+    dl = F.deltas(dt, dt_bias)
+    starts = [cache[2], np.zeros((Dc, N))]
+    ends = []
+    for r, segs in ((0, [(0, 5), (5, 13)]), (1, [(13, 16), (16, 20)])):
+        h = starts[r]
+        for a, b in segs:
+            yq, h = F.mamba1_quadratic(x[a:b], dl[a:b], A, B[a:b], C[a:b], D, h)
+            assert F.rel_err(y[a:b], yq) < 1e-12
+            ends.append(h)
+    assert F.rel_err(new[2], ends[0]) < 1e-12
+    assert F.rel_err(new[5], ends[1]) < 1e-12
+    assert F.rel_err(new[6], ends[3]) < 1e-12
+    for s in (0, 1, 3, 4, 7):
+        assert np.array_equal(new[s], cache[s]), s

@@ -424,3 +424,54 @@ def test_conv1d_resume_from_state_and_chunk_states(oracle_lib):
     oa, fa, _ = oracle_lib.causal_conv1d_varlen(xa, w, None, [0, 7])
     ob, fb, _ = oracle_lib.causal_conv1d_varlen(xb, w, None, [0, 12])
     assert np.array_equal(packed, np.concatenate([oa, ob])) and np.array_equal(fp, np.concatenate([fa, fb]))
+
+
+@pytest.mark.parametrize("null", [0, -1])
+def test_conv1d_cache_routing_hand_written(oracle_lib, null):
+    """Pin 13c: slot routing of the conv-state cache ("vLLM v0.20.0 하이브리드 SSM
+    모델을 위한 분산 서빙 추가", "전체 흐름": one [state_len, conv_dim] conv state
+    per cache block), on hand-written slot lists whose expected contents are
+    read off the inputs by eye.
+
+    Token t holds 100 (t + 1) + c in channel c, and slot s starts as
+    -(10 s + 1 .. 4), so every stored row names where it came from.  W = 3,
+    so a state is the last two input rows.  Sequence 0 reads its initial
+    state from slot 3 and also writes its final state there (read before
+    write); sequence 1 has a null initial slot (zeros); sequence 2 reads slot
+    4, which its own first chunk then overwrites; one chunk slot and one
+    output slot are null; the slots no one writes keep their bits."""
+    W, D = 3, 2
+    cu = [0, 5, 6, 9]
+    cc = [0, 2, 5, 6, 7, 9]
+    x = np.array([[100.0 * (t + 1) + c for c in range(D)] for t in range(9)])
+    cache = np.array([[[-(10.0 * s + 1), -(10.0 * s + 2)], [-(10.0 * s + 3), -(10.0 * s + 4)]]
+                      for s in range(10)])
+    init_slot = [3, null, 4]
+    out_slot = [3, 6, null]
+    chunk_slot = [7, null, 8, 4, 9]
+    w = np.array([[0.5, -1.0, 2.0], [0.25, 3.0, -0.5]])
+    b = np.array([0.125, -2.0])
+    out, new = oracle_lib.causal_conv1d_with_cache(x, w, b, cu, cache, init_slot, out_slot, null,
+                                                   activation="none", cu_chunk_seqlens=cc,
+                                                   chunk_slot=chunk_slot)
+    want = {
+        7: [[100, 101], [200, 201]],      # chunk 0 of sequence 0 ends at token 1
+        3: [[400, 401], [500, 501]],      # sequence 0's final state, over its initial slot
+        8: [[0, 0], [600, 601]],          # chunk 2 = all of sequence 1, zero history
+        6: [[0, 0], [600, 601]],          # sequence 1's final state
+        4: [[-43, -44], [700, 701]],      # chunk 3: sequence 2's history row 2, then token 6
+        9: [[800, 801], [900, 901]],      # chunk 4
+    }
+    for s in range(10):
+        if s in want:
+            assert np.array_equal(new[s], np.array(want[s], np.float64)), s
+        else:
+            assert np.array_equal(new[s], cache[s]), s
+    # outputs: numpy's convolution over [history; tokens] of each sequence, where the
+    # history is the hand-chosen slot's original rows (zeros for the null slot)
+    hist = [cache[3], np.zeros((2, D)), cache[4]]
+    for r in range(3):
+        buf = np.concatenate([hist[r], x[cu[r]:cu[r + 1]]])
+        L = cu[r + 1] - cu[r]
+        ref = np.stack([np.convolve(buf[:, c], w[c, ::-1])[W - 1:W - 1 + L] + b[c] for c in range(D)], axis=1)
+        assert np.allclose(out[cu[r]:cu[r + 1]], ref, rtol=1e-15, atol=1e-12), r
