@@ -390,9 +390,24 @@ def conv1d_leg(st, steps, warmup):
     ms = e0.elapsed_time(e1) / steps
     nbytes = 2 * T * D * 2 + st.K * (W - 1) * D * 2 + S * (W - 1) * D * 2 + D * (W + 1) * 4
     hbm, _ = _peaks()
+    # the decode form on the step's single-token requests: each continues the conv state in its slot
+    R = st.dec["live"]
+    dec = None
+    if R > 0:
+        xd = torch.randn(R, D, generator=g, device=st.dev).to(torch.bfloat16)
+        si = st.si_dev[:, 0].contiguous()
+        douts = st.ssd._binding._conv_outputs(xd, dim_x, dim_bc, None, None, None)
+
+        def dcall():
+            ssd.ssd_conv1d_update(xd, weight, state, si, dim_x, dim_bc, bias=bias, null_block_id=p["null_block_id"],
+                                  x_out=douts[0], B_out=douts[1], C_out=douts[2])
+        dms = _flushed_ms(st.dev, dcall)
+        dbytes = 2 * R * D * 2 + 2 * R * (W - 1) * D * 2 + D * (W + 1) * 4
+        dec = {"requests": R, "ms_l2_flushed": dms, "algorithmic_bytes": dbytes,
+               "hbm_frac_l2_flushed": dbytes / (dms * 1e-3) / 1e9 / hbm}
     return {"what": "depthwise causal conv1d, W=4, silu, %d channels (x %d, B and C %d each)" % (D, dim_x, dim_bc),
             "ms": ms, "tokens_per_s": T / (ms * 1e-3), "algorithmic_bytes": nbytes,
-            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "kernels": 2}
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "kernels": 2, "decode": dec}
 
 
 MAMBA1_SHAPE = dict(num_seqs=8, seq_len=8192, dim=5120, dstate=16, ngroups=1, chunk_size=2048, decodes=256)
@@ -464,6 +479,152 @@ def mamba1_leg(dev, steps, warmup):
             "decode": {"requests": R, "ms": dms, "state_updates_per_s": R / (dms * 1e-3), "algorithmic_bytes": dbytes,
                        "hbm_frac": dbytes / (dms * 1e-3) / 1e9 / hbm},
             "kernels": 2}
+
+
+# ------------------------------------------------------- the other configs --
+
+L2_FLUSH_BYTES = 512 << 20  # written between repetitions where a config's data fits in the 129 MB L2
+
+
+def _graph_ms(dev, call, per_graph=20, min_s=0.4):
+    """Per-call device time of ``call`` replayed back to back: ``per_graph`` calls captured in one
+    CUDA graph (so host work between calls cannot leave the GPU idle), the graph replayed until
+    ``min_s`` seconds of device time have passed, CUDA events around the replays."""
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            call()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    reps = max(1, int(min_s * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * per_graph)
+
+
+def _flushed_ms(dev, call, reps=40):
+    """Median device time of one call with L2 flushed before it: each call sits between CUDA events,
+    after a write of L2_FLUSH_BYTES.  A spin kernel first lets the host queue every repetition, so
+    the device never waits on the host inside a timed pair."""
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda._sleep(200_000_000)
+    for a, b in evs:
+        flush.fill_(1.0)
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def configs_leg(dev):
+    """The other workloads of the path, each on its own: the single-sequence warm-up shape
+    (2048 tokens = one chunk, H=48, P=64, N=128, G=4; with and without an initial state; L2 flushed
+    and not, since its 31 MB fit in L2), the varlen prefix-cached batch (32 requests, U(64,4096) new
+    tokens, U(0,8192) computed, chunk 256, half resuming from a 4096-slot cache) and the
+    speculative-decode batch (256 live requests padded to 512, 1+3 tokens, U{0..3} accepted, in place
+    on an 8192-slot cache; L2 flushed).  Per config: device ms per call, its algorithmic HBM bytes,
+    their fraction of the measured copy bandwidth, and the clocks seen while it ran."""
+    import selective_state_space_mamba2_gb300 as ssd
+    from selective_state_space_mamba2_gb300 import workloads as W
+    hbm, _ = _peaks()
+    out = {}
+
+    def prefill_call(c):
+        meta = ssd.ssd_chunk_metadata(c["cu_seqlens"], c["chunk_size"], c["num_computed"], c["has_init"],
+                                      block_table=c["block_table"], state_indices=c["state_indices"],
+                                      null_block_id=c["null_block_id"])
+        m = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in meta.items()}
+        cu = c["cu_seqlens"].to(dev)
+        y = torch.empty_like(c["x"])
+        a = ssd.prefill_args(c["x"], c["dt"], c["A"], c["B"], c["C"], cu, m["cu_chunk_seqlens"], m["seq_idx"],
+                             m["last_chunk_indices"], y, m["init_slot"], m["chunk_slot"], c["cache"], c["D"],
+                             c["dt_bias"], chunk_size=c["chunk_size"], seq_order=m["seq_order"])
+        ws = torch.empty(max(ssd.ssd_prefill_workspace_size(a), 1), dtype=torch.uint8, device=dev)
+        K = int(meta["cu_chunk_seqlens"].shape[0] - 1)
+        inits = int(sum(int(v) != c["null_block_id"] for v in meta["init_slot"]))
+
+        def call():
+            ssd.ssd_prefill_varlen(c["x"], c["dt"], c["A"], c["B"], c["C"], cu, m["cu_chunk_seqlens"], m["seq_idx"],
+                                   m["last_chunk_indices"], out=y, init_slot=m["init_slot"],
+                                   chunk_slot=m["chunk_slot"], state_cache=c["cache"], D=c["D"],
+                                   dt_bias=c["dt_bias"], null_block_id=c["null_block_id"],
+                                   chunk_size=c["chunk_size"], workspace=ws, seq_order=m["seq_order"])
+        return call, K, inits, ssd.ssd_prefill_kernel_count(a)
+
+    def entry(T, nbytes, ms, extra=None):
+        d = {"ms": ms, "tokens_per_s_per_layer": T / (ms * 1e-3), "algorithmic_bytes": nbytes,
+             "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm}
+        d.update(extra or {})
+        return d
+
+    warm = {"workload": "single-sequence warm-up shape: 2048 tokens = chunk_size, batch 1, H=48, P=64, N=128, G=4, bf16"}
+    for name, with_init in (("no_init", False), ("with_init", True)):
+        c = W.warmup_shape_prefill(dev, with_init=with_init)
+        H, P, N, G = c["x"].shape[1], c["x"].shape[2], c["B"].shape[2], c["B"].shape[1]
+        call, K, inits, nk = prefill_call(c)
+        nbytes = prefill_bytes(2048, K, H, P, N, G, 2, init_reads=inits)
+        with ClockSampler(dev.index) as clk:
+            ms = _graph_ms(dev, call)
+            msf = _flushed_ms(dev, call)
+        warm[name] = entry(2048, nbytes, ms, {"ms_l2_flushed": msf, "hbm_frac_l2_flushed":
+                                              nbytes / (msf * 1e-3) / 1e9 / hbm, "kernels": nk,
+                                              "clocks": clk.summary()})
+        del c, call
+    out["warmup_2048"] = warm
+
+    c = W.varlen_prefix_cached_prefill(dev)
+    H, P, N, G = c["x"].shape[1], c["x"].shape[2], c["B"].shape[2], c["B"].shape[1]
+    T = int(c["cu_seqlens"][-1])
+    call, K, inits, nk = prefill_call(c)
+    nbytes = prefill_bytes(T, K, H, P, N, G, 2, init_reads=inits)
+    with ClockSampler(dev.index) as clk:
+        ms = _graph_ms(dev, call, per_graph=10)
+    out["varlen_prefix_cached"] = entry(T, nbytes, ms, {
+        "workload": "varlen prefix-cached prefill: 32 requests, new U(64,4096), computed U(0,8192), chunk 256, "
+                    "half resuming from a [4096,48,64,128] cache; %d tokens, %d chunks, %d initial states"
+                    % (T, K, inits), "kernels": nk, "l2": "inputs larger than L2 (no flush)", "clocks": clk.summary()})
+    del c, call
+
+    d = W.spec_decode_batch(dev)
+    H, P, N, G = d["x"].shape[1], d["x"].shape[2], d["B"].shape[2], d["B"].shape[1]
+    si, na = d["state_indices"].to(dev), d["num_accepted"].to(dev)
+    yd = torch.empty_like(d["x"])
+    tpr = d["tokens_per_req"]
+    writes = int((d["state_indices"][:d["live"], :tpr] != d["null_block_id"]).sum())
+
+    def dcall():
+        ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], si, na, out=yd, D=d["D"],
+                              dt_bias=d["dt_bias"], null_block_id=d["null_block_id"])
+    nbytes = decode_bytes(d["live"], tpr, writes, H, P, N, G, 2)
+    with ClockSampler(dev.index) as clk:
+        msf = _flushed_ms(dev, dcall)
+    ups = d["live"] * tpr
+    out["spec_decode"] = {"workload": "speculative decode: 256 live requests padded to 512 (null rows), 1+3 tokens, "
+                                      "num_accepted U{0..3}, in place on an [8192,48,64,128] fp32 cache",
+                          "ms_l2_flushed": msf, "state_updates_per_s": ups / (msf * 1e-3), "algorithmic_bytes": nbytes,
+                          "hbm_frac_l2_flushed": nbytes / (msf * 1e-3) / 1e9 / hbm, "kernels": 1,
+                          "clocks": clk.summary()}
+    return out
 
 
 def _barrier(dist_on):
@@ -572,6 +733,7 @@ def gpu_arm(args, rank, world, dist_on):
 
     conv = None if args.no_conv else conv1d_leg(st, args.steps, args.warmup)
     m1 = None if args.no_mamba1 else mamba1_leg(dev, args.steps, args.warmup)
+    cfgs = None if args.no_configs else configs_leg(dev)
     if rank != 0:
         return None
     hbm, peak_kind = _peaks()
@@ -613,6 +775,7 @@ def gpu_arm(args, rank, world, dist_on):
         "gpu_launches": (st.prefill_kernels + (1 if R else 0)) * args.steps,
         "conv1d": conv,
         "mamba1": m1,
+        "configs": cfgs,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -698,6 +861,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiler runs)")
     ap.add_argument("--no-conv", action="store_true", help="skip the conv1d measurement")
     ap.add_argument("--no-mamba1", action="store_true", help="skip the Mamba1 measurement")
+    ap.add_argument("--no-configs", action="store_true", help="skip the warm-up, varlen and spec-decode configs")
     ap.add_argument("--serial-step", action="store_true", help="run the step's decode after the prefill on one stream")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -82,7 +82,7 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype_t;
 SSD_API const char *ssd_status_string(ssd_status_t status);
 
 /* ABI version of this header; bumped on any incompatible change. */
-#define SSD_ABI_VERSION 1
+#define SSD_ABI_VERSION 2
 SSD_API int32_t ssd_abi_version(void);
 
 /* ------------------------------------------------------------------------ *
@@ -200,7 +200,15 @@ typedef struct ssd_prefill_args {
     uint32_t *err_word;        /* device word or NULL */
     const int32_t *seq_order;  /* [S] device, a permutation of 0..S-1 giving the order in which
                                   sequences are started (longest first balances the GPU), or
-                                  NULL for index order; results do not depend on it */
+                                  NULL for index order; results do not depend on it.  An entry
+                                  outside [0, S) or repeated sets SSD_DEVERR_METADATA (a repeated
+                                  entry leaves the y of the sequence it displaced unwritten) */
+    int64_t wait_limit_cycles; /* watchdog of the tensor-core kernel: SM clock cycles any of its
+                                  device-side waits (for a copy, a product or another warp) may
+                                  take before the CTA sets SSD_DEVERR_TIMEOUT, lets its own copies
+                                  and products finish, frees its tensor memory and exits; 0 selects
+                                  the default of 2e9 (about a second).  The CUDA-core kernels have
+                                  no such waits and ignore it. */
 } ssd_prefill_args;
 
 /* Bytes of device workspace ssd_prefill_varlen needs for these arguments

@@ -38,7 +38,8 @@ class PrefillArgs(ctypes.Structure):
                 ("x", _vp), ("dt", _vp), ("B", _vp), ("C", _vp), ("z", _vp), ("A", _vp), ("D", _vp),
                 ("dt_bias", _vp), ("cu_seqlens", _vp), ("cu_chunk_seqlens", _vp), ("seq_idx", _vp),
                 ("last_chunk_indices", _vp), ("init_slot", _vp), ("chunk_slot", _vp),
-                ("state_cache", _vp), ("y", _vp), ("err_word", _vp), ("seq_order", _vp)]
+                ("state_cache", _vp), ("y", _vp), ("err_word", _vp), ("seq_order", _vp),
+                ("wait_limit_cycles", ctypes.c_int64)]
 
 
 class DecodeArgs(ctypes.Structure):
@@ -209,7 +210,7 @@ def ssd_chunk_metadata(cu_seqlens, chunk_size, num_computed_tokens=None, has_ini
 def prefill_args(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices, out,
                  init_slot=None, chunk_slot=None, state_cache=None, D=None, dt_bias=None, z=None,
                  dt_softplus=True, dt_limit=(0.0, math.inf), null_block_id=0, chunk_size=None,
-                 err_word=None, seq_order=None):
+                 err_word=None, seq_order=None, wait_limit_cycles=0):
     """Fills a ``PrefillArgs`` from device tensors (validating shapes and dtypes)."""
     T, H, P = x.shape
     G, N = B.shape[1], B.shape[2]
@@ -245,6 +246,7 @@ def prefill_args(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chu
         a.num_slots = state_cache.shape[0]
     a.err_word = _dev(err_word, "err_word", required=False)
     a.seq_order = _dev(seq_order, "seq_order", torch.int32, required=False)
+    a.wait_limit_cycles = int(wait_limit_cycles)
     if a.chunk_size == 0:
         a.chunk_size = 1
     return a
@@ -262,7 +264,7 @@ def ssd_prefill_varlen(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, la
                        out=None, init_slot=None, chunk_slot=None, state_cache=None, D=None,
                        dt_bias=None, z=None, dt_softplus=True, dt_limit=(0.0, math.inf),
                        null_block_id=0, chunk_size=None, workspace=None, err_word=None, stream=None,
-                       seq_order=None):
+                       seq_order=None, wait_limit_cycles=0):
     """Varlen SSD prefill on device tensors; returns ``out`` ([T,H,P], x's dtype).
 
     ``workspace`` (uint8 CUDA tensor) is allocated with torch when omitted.
@@ -271,7 +273,7 @@ def ssd_prefill_varlen(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, la
         out = torch.empty_like(x)
     a = prefill_args(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices, out,
                      init_slot, chunk_slot, state_cache, D, dt_bias, z, dt_softplus, dt_limit,
-                     null_block_id, chunk_size, err_word, seq_order)
+                     null_block_id, chunk_size, err_word, seq_order, wait_limit_cycles)
     need = ssd_prefill_workspace_size(a)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)

@@ -24,6 +24,7 @@ ssd_status_t check_prefill(const ssd_prefill_args *a) {
     if (a->total_tokens < 0 || a->num_seqs < 0 || a->num_chunks < 0) return SSD_ERR_INVALID_ARG;
     if (!dims_ok(a->nheads, a->headdim, a->dstate, a->ngroups)) return SSD_ERR_INVALID_ARG;
     if (!dtype_ok(a->dtype) || !limits_ok(a->dt_min, a->dt_max)) return SSD_ERR_INVALID_ARG;
+    if (a->wait_limit_cycles < 0) return SSD_ERR_INVALID_ARG;
     if (a->num_chunks > 0 && (a->total_tokens == 0 || a->num_seqs == 0)) return SSD_ERR_INVALID_ARG;
     if (a->total_tokens > 0 && a->num_chunks == 0) return SSD_ERR_INVALID_ARG;
     if (a->total_tokens == 0) return SSD_OK;

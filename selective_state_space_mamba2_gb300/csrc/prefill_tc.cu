@@ -61,6 +61,7 @@ struct TcParams {
     __nv_bfloat16 *y;
     uint32_t *err;
     const int32_t *seq_order;
+    long long wait_limit;  // cycles a device-side wait may take before the CTA gives up
 };
 
 namespace {
@@ -127,9 +128,9 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool v) {
 }
 
 // One lane per warp polls the barrier; the warp learns the outcome by shuffle.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, long long limit) {
     bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity);
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, limit);
     ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
     __syncwarp();
     return ok;
@@ -251,7 +252,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------ TMA producer ----
-        if (lane == 0) {
+        if (lane != 0) {
+            // The idle lanes check, for one head of each sequence, that seq_order names this
+            // sequence exactly once (with every entry in range, a permutation then follows): a
+            // repeated entry would run one sequence twice and leave another's y unwritten.
+            if (h == 0 && p.seq_order) {
+                int cnt = 0;
+                for (int i = lane - 1; i < p.S; i += 31) cnt += p.seq_order[i] == r;
+                cnt = __reduce_add_sync(0xfffffffeu, cnt);
+                if (lane == 1 && cnt != 1) report(p.err, SSD_DEVERR_METADATA);
+            }
+        } else {
             // Two rings, each refilled as soon as its slot frees: C/B tiles once M3 of the
             // block two back is done, x tiles once y of the block three back is out.
             Cursor ccb, cx;
@@ -287,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (prog) {
                     t_prog = clock64();
-                } else if (clock64() - t_prog > 2000000000ll) {
+                } else if (clock64() - t_prog > p.wait_limit) {
                     report(p.err, SSD_DEVERR_TIMEOUT);
                     break;
                 } else if (ncb < nblocks) {
@@ -328,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&bar[S_RDY0 + sb]);
             };
-            bool ok = mbar_wait(&bar[FULL_CB0], 0);
+            bool ok = mbar_wait(&bar[FULL_CB0], 0, p.wait_limit);
             if (ok) {
                 tc_fence_after();
                 issue_m1(0);
@@ -340,14 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dCs = s ? dC1 : dC0, dBms = s ? dBm1 : dBm0;
                 const uint64_t dXs = xs == 0 ? dX0 : (xs == 1 ? dX1 : dX2);
                 // M4: dS = B^T (w x) once w x exists and dS of the previous block was read
-                if (!(ok = mbar_wait(&bar[OPS_W], i & 1)) || !(ok = mbar_wait(&bar[DS_FREE], i & 1))) break;
+                if (!(ok = mbar_wait(&bar[OPS_W], i & 1, p.wait_limit)) || !(ok = mbar_wait(&bar[DS_FREE], i & 1, p.wait_limit))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_ss(tm + COL_DS, desc_at(dBms, 2048 * k), desc_at(dXW, 2048 * k), kIdD, k > 0);
                 mma_commit(&bar[ACC_DS]);
                 // M3: Y2 = C Hprev^T once the state entering the block exists
-                if (!(ok = mbar_wait(&bar[OPS_H], i & 1))) break;
+                if (!(ok = mbar_wait(&bar[OPS_H], i & 1, p.wait_limit))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -357,14 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bar[H_FREE]);
                 mma_commit(&bar[EMPTY_CB0 + s]);  // M1, M4 and M3 of the block have read its C/B stage
                 // M2: Y1 = P X once P is ready and Y1 of the previous block was read
-                if (!(ok = mbar_wait(&bar[PRDY0 + s], (i >> 1) & 1)) || !(ok = mbar_wait(&bar[Y1_FREE], i & 1))) break;
+                if (!(ok = mbar_wait(&bar[PRDY0 + s], (i >> 1) & 1, p.wait_limit)) || !(ok = mbar_wait(&bar[Y1_FREE], i & 1, p.wait_limit))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_ts(tm + COL_Y1, tm + (s ? COL_S1 : COL_S0) + 8 * k, desc_at(dXs, 2048 * k), kIdY, k > 0);
                 mma_commit(&bar[ACC_Y]);
                 if (i + 1 < nblocks) {
-                    if (!(ok = mbar_wait(&bar[FULL_CB0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1))) break;
+                    if (!(ok = mbar_wait(&bar[FULL_CB0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1, p.wait_limit))) break;
                     tc_fence_after();
                     issue_m1(i + 1);
                 }
@@ -428,29 +439,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t w2 = pack_f16_sat(__expf(c_last - c) * delta, __expf(c_last - c) * delta);
 
             // ---- w x (fp16) into the M4 operand once M4 of the previous block is done; x -> fp16
-            bool ok = warp_wait(&bar[FULL_X0 + i % kXStages], (i / kXStages) & 1);
-            if (ok && i > 0) ok = warp_wait(&bar[ACC_DS], (i - 1) & 1);
+            bool ok = warp_wait(&bar[FULL_X0 + i % kXStages], (i / kXStages) & 1, p.wait_limit);
+            if (ok && i > 0) ok = warp_wait(&bar[ACC_DS], (i - 1) & 1, p.wait_limit);
             if (!named_bar_and(BAR_PG, 128, ok)) {
                 if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
             }
+            // Rows t >= L hold the next sequence's tokens (the TMA box is always 128 rows): they are
+            // replaced by zeros, not scaled by w = 0, so a non-finite value there cannot reach this
+            // sequence's products (0 * inf is NaN).
+            const bool live = t < L;
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
-                const uint4 xh = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(sXs + sw128_offset(t, cc)));
-                const uint4 xw = make_uint4(hmul2_u32(xh.x, w2), hmul2_u32(xh.y, w2), hmul2_u32(xh.z, w2),
-                                            hmul2_u32(xh.w, w2));
+                uint4 xh = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(sXs + sw128_offset(t, cc)));
+                uint4 xw = make_uint4(hmul2_u32(xh.x, w2), hmul2_u32(xh.y, w2), hmul2_u32(xh.z, w2),
+                                      hmul2_u32(xh.w, w2));
+                if (!live) xh = xw = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
                 *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = xh;
+            }
+            bool s_ready = false;
+            if (L < kL) {
+                // A short block: M4 sums B rows against w x over all 128 rows, so B's rows past the
+                // block end are cleared too, once M1 (the other reader of the stage) is done with them.
+                ok = warp_wait(&bar[S_RDY0 + s], ph, p.wait_limit);
+                if (!named_bar_and(BAR_PG, 128, ok)) {
+                    if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+                    break;
+                }
+                s_ready = true;
+                if (!live) {
+                    uint8_t *sB = stage_b(s);
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        *reinterpret_cast<uint4 *>(sB + sw128_offset(t, cc)) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(sB + 16384 + sw128_offset(t, cc)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[OPS_W]);
 
             // ---- S ready: P pass, S (fp32) -> P (fp16) over the same columns
-            ok = warp_wait(&bar[S_RDY0 + s], ph);
-            if (!named_bar_and(BAR_PG, 128, ok)) {
-                if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
-                break;
+            if (!s_ready) {
+                ok = warp_wait(&bar[S_RDY0 + s], ph, p.wait_limit);
+                if (!named_bar_and(BAR_PG, 128, ok)) {
+                    if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+                    break;
+                }
             }
             tc_fence_after();
             // Group j of P goes over columns [16j, 16j+16), which hold S groups <= j that this
@@ -543,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = i & 1;
             const int tb = cur.tb, L = cur.len();
             // ---- dS: the state after this block, then the fp16 state for the next block's M3
-            bool ok = warp_wait(&bar[ACC_DS], i & 1);
+            bool ok = warp_wait(&bar[ACC_DS], i & 1, p.wait_limit);
             if (!named_bar_and(BAR_CG, 128, ok)) {
                 if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
@@ -561,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[DS_FREE]);  // M4 of the next block may overwrite dS
-            ok = warp_wait(&bar[H_FREE], i & 1);          // M3 of this block has read the state tile
+            ok = warp_wait(&bar[H_FREE], i & 1, p.wait_limit);         // M3 of this block has read the state tile
             if (!named_bar_and(BAR_CG, 128, ok)) {
                 if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
@@ -579,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.chunk_slot) cs = p.chunk_slot[min(cur.k + 1, last)];
             }
             // ---- y = Y1 + exp(c_t) Y2
-            ok = warp_wait(&bar[ACC_Y], i & 1);
+            ok = warp_wait(&bar[ACC_Y], i & 1, p.wait_limit);
             if (!named_bar_and(BAR_CG, 128, ok)) {
                 if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
                 break;
@@ -706,6 +743,7 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
     p.y = static_cast<__nv_bfloat16 *>(a.y);
     p.err = a.err_word;
     p.seq_order = a.seq_order;
+    p.wait_limit = a.wait_limit_cycles > 0 ? (long long)a.wait_limit_cycles : 2000000000ll;
     auto kernel = p.z ? ssd_prefill_tc_kernel<true> : ssd_prefill_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;

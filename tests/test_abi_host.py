@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(B.EXPORTED_SYMBOLS) <= set(declared)
     for name in declared:
         assert hasattr(lib, name), name
-    assert lib.ssd_abi_version() == 1
+    assert lib.ssd_abi_version() == 2
     assert lib.ssd_status_string(3) == b"SSD_ERR_WORKSPACE"
 
 
@@ -112,6 +112,7 @@ def _prefill_args(**over):
     (dict(dt_min=1.0, dt_max=0.5), B.SSD_ERR_INVALID_ARG),
     (dict(num_chunks=0), B.SSD_ERR_INVALID_ARG),
     (dict(init_slot=0x10000), B.SSD_ERR_INVALID_ARG),  # slots without a cache
+    (dict(wait_limit_cycles=-1), B.SSD_ERR_INVALID_ARG),
 ])
 def test_prefill_host_validation(lib, over, code):
     a = _prefill_args(**over)

@@ -174,3 +174,82 @@ def test_output_gate(dtype):
     g = torch.Generator(device=DEV).manual_seed(99)
     z = (3.0 * torch.randn(case["x"].shape, generator=g, device=DEV)).to(dtype)
     _run_and_check(case, z=z)
+
+
+def test_tensor_core_path_without_D_and_bias_with_dt_limit():
+    """The tensor-core kernel (bf16, headdim 64, dstate 128) with D and
+    dt_bias absent and a dt_limit clamp that binds at both ends, on the ragged
+    batch (partial blocks, unaligned first chunks, an empty sequence)."""
+    new = [300, 1, 0, 129, 64, 517]
+    nc = [10, 64, 0, 63, 0, 200]
+    case = W.prefill_case(17, new, nc, 4, 64, 128, 2, 64, device=DEV,
+                          has_init=[True, True, False, False, False, True], num_slots=200)
+    _run_and_check(case, D=None, dt_bias=None, dt_limit=(0.05, 0.4))
+
+
+def test_tensor_core_path_large_delta():
+    """Step sizes of 200-300 (dt + dt_bias far above 15, the branch where
+    softplus is the identity) with slow decay rates A = -exp(U(-7,-5)), so a
+    token's contribution survives a few tokens: the fp16 operands P (up to
+    about |C.B| * delta, ~2e4), w x and the carried state run near, but
+    inside, the fp16 range."""
+    case = W.prefill_case(18, [700, 190], [0, 0], 4, 64, 128, 2, 256, device=DEV, num_slots=40)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    case["A"] = -torch.exp(-7.0 + 2.0 * torch.rand(4, generator=g, device=DEV))
+    bias = 200.0 + 100.0 * torch.rand(4, generator=g, device=DEV)
+    _run_and_check(case, dt_bias=bias)
+
+
+def test_non_finite_tokens_of_the_next_sequence_stay_out():
+    """The last block of sequence 0 is short (200 = 128 + 72 tokens), so the
+    128-row tiles of that block also hold sequence 1's first 56 tokens.  Those
+    hold inf and NaN in x, B, C and dt: sequence 0's y and stored states must
+    stay finite and at parity with the oracle on sequence 0 alone."""
+    case = W.prefill_case(19, [200, 300], [0, 0], 4, 64, 128, 2, 256, device=DEV, num_slots=40)
+    ref = {k: case[k].clone() for k in ("x", "B", "C", "dt")}
+    case["x"][200:256] = float("nan")
+    case["x"][230:240, 1] = float("inf")
+    case["B"][200:256] = float("inf")
+    case["B"][220:230, 0] = -float("inf")
+    case["C"][200:256] = float("nan")
+    case["dt"][200:256] = float("inf")
+    before = case["cache"].clone()
+    err = _err()
+    y, meta = PT.run_prefill(case, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    k0 = int(meta["last_chunk_indices"][0]) + 1  # chunks of sequence 0
+    assert torch.isfinite(y[:200]).all()
+    slots0 = [int(s) for s in meta["chunk_slot"][:k0]]
+    assert torch.isfinite(case["cache"][slots0]).all()
+    # oracle on sequence 0 alone, with its (finite) tokens
+    one = dict(case, x=ref["x"][:200], B=ref["B"][:200], C=ref["C"][:200], dt=ref["dt"][:200],
+               cu_seqlens=torch.tensor([0, 200], dtype=torch.int32))
+    m0 = {"cu_chunk_seqlens": meta["cu_chunk_seqlens"][:k0 + 1], "init_slot": meta["init_slot"][:1]}
+    yo, cso = PT.oracle_prefill(one, m0, before)
+    tol = PT.TOL[torch.bfloat16]
+    assert PT.y_err(y[:200].double().cpu().numpy(), yo, torch.bfloat16) <= tol
+    assert PT.rel_err(case["cache"][slots0].double().cpu().numpy(), cso) <= tol
+
+
+def test_repeated_seq_order_entry_is_reported():
+    case = W.prefill_case(20, [150, 90], [0, 0], 4, 64, 128, 2, 64, device=DEV, num_slots=20)
+    meta = PT.prefill_metadata(case)
+    meta["seq_order"] = np.array([0, 0], np.int32)
+    err = _err()
+    PT.run_prefill(case, meta=meta, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ssd.DEVERR_METADATA
+
+
+def test_bounded_waits_give_up_and_the_context_survives():
+    """With a watchdog of 100 cycles every CTA's first wait for a tile gives
+    up: the call returns, SSD_DEVERR_TIMEOUT is set, and the next call (the
+    default watchdog) on the same context is correct."""
+    case = W.prefill_case(21, [300, 129], [0, 0], 4, 64, 128, 2, 64, device=DEV, num_slots=40)
+    err = _err()
+    PT.run_prefill(case, err=err, wait_limit_cycles=100)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ssd.DEVERR_TIMEOUT
+    case["cache"] = W.sentinel_cache(40, 4, 64, 128, DEV)
+    _run_and_check(case)
