@@ -214,7 +214,8 @@ typedef struct ssd_prefill_args {
 /* Bytes of device workspace ssd_prefill_varlen needs for these arguments
  * (sizes only are read).  0 on invalid sizes.  With up256 rounding up to a
  * multiple of 256: bf16 with headdim 64 and dstate 128 (the tensor-core
- * kernel) needs the fp16 copies of B and C, 2*up256(2*T*G*N) bytes; every
+ * kernel) needs the fp16 copies of B and C and, per head and token, delta and
+ * its in-block cumsum: 2*up256(2*T*G*N) + 2*up256(4*H*T) bytes; every
  * other case (the CUDA-core path) needs up256(4*H*T) + up256(8*H*T) +
  * 2*up256(4*K*H*P*N) for delta, the fp64 cumsum, the chunk states and the
  * states entering each chunk. */

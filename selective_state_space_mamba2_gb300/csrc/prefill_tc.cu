@@ -8,11 +8,12 @@
 // end of every chunk is stored to its cache slot (prefix caching, "청크 기반
 // 프리픽스 캐싱" on "[vLLM] Mamba (SSM): 선형 시간 복잡도 시퀀스 모델링").
 //
-// Per block of L <= 128 tokens [tb, tb+L) with in-block cumsum c_t of
-// delta*A, the four dense contractions run as tcgen05.mma tiles with fp32
-// accumulators and fp16 operands (B and C are converted once per call by a
-// small kernel; x, P, w x and the carried state are rounded to fp16, whose
-// 11-bit significand keeps their rounding error 8x below bf16's):
+// A small kernel in front (prep_kernel) converts B and C to fp16 once per call
+// and writes delta and its in-block cumsum c for every head and token.  Per
+// block of L <= 128 tokens [tb, tb+L), the four dense contractions run as
+// tcgen05.mma tiles with fp32 accumulators and fp16 operands (x, P, w x and
+// the carried state are rounded to fp16, whose 11-bit significand keeps their
+// rounding error 8x below bf16's):
 //   M1  S  = C B^T                  [128 x 128], K = dstate   (SS, K/K-major)
 //   M2  Y1 = P X                    [128 x  64], K = tokens   (TS: P in TMEM)
 //        P[t,s] = exp(c_t - c_s) delta_s S[t,s] for s <= t, plus D on the diagonal
@@ -27,8 +28,8 @@
 //
 // Only the state itself is a serial dependency from block to block (64 FMAs
 // per thread); everything else is pipelined.  One CTA per SM, 320 threads:
-//   warps 0-3  "producer" warpgroup, one block ahead: delta and the cumsum,
-//              w x and x -> fp16, the P pass (S -> P in TMEM, in place)
+//   warps 0-3  "producer" warpgroup, one block ahead: the column factors from
+//              delta and c, w x and x -> fp16, the P pass (S -> P in TMEM, in place)
 //   warps 4-7  "consumer" warpgroup: state update, the fp16 state tile for
 //              the next block's M3, the chunk-boundary stores, y and its
 //              coalesced copy-out
@@ -62,6 +63,8 @@ struct TcParams {
     uint32_t *err;
     const int32_t *seq_order;
     long long wait_limit;  // cycles a device-side wait may take before the CTA gives up
+    const float *cum;      // [H, T] in-block inclusive cumsum of delta * A (written by prep_kernel)
+    const float *delta;    // [H, T] delta (written by prep_kernel)
 };
 
 namespace {
@@ -86,12 +89,10 @@ constexpr int kCbStages = 2, kXStages = 3;
 constexpr uint32_t OFF_X = kCbStages * CB_STAGE;
 constexpr uint32_t OFF_XW = OFF_X + kXStages * X_STAGE;  // w x (fp16)
 constexpr uint32_t OFF_H = OFF_XW + 16384;   // fp16 state entering the block
-constexpr uint32_t OFF_F = OFF_H + 16384;    // column factors [128]
-constexpr uint32_t OFF_CD = OFF_F + 512;     // c_t and delta_t [2][128]
-constexpr uint32_t OFF_E = OFF_CD + 1024;    // exp(c_t) per block, ring of 4 [4][128]
+constexpr uint32_t OFF_F = OFF_H + 16384;    // column factors, c_t and delta_t: [2 blocks][3][128]
+constexpr uint32_t OFF_E = OFF_F + 3072;     // exp(c_t) per block, ring of 4 [4][128]
 constexpr uint32_t OFF_DEC = OFF_E + 2048;   // exp(c_L) per block, ring of 4
-constexpr uint32_t OFF_WT = OFF_DEC + 16;    // warp sums of delta*A [4]
-constexpr uint32_t OFF_TM = OFF_WT + 16;     // TMEM base address
+constexpr uint32_t OFF_TM = OFF_DEC + 16;    // TMEM base address
 constexpr uint32_t OFF_BAR = OFF_TM + 16;    // mbarriers
 constexpr uint32_t kSmemBytes = OFF_BAR + 24 * 8;
 constexpr int kRing = 4;
@@ -163,6 +164,19 @@ struct Cursor {
     }
 };
 
+// What the producer warpgroup needs of row t of a block [tb, tb + L): delta, the in-block
+// cumsum, and the cumsum at the end of each 32-row group (row min(32 j + 31, L - 1)).
+struct RowVals {
+    float c, d, g[4];
+    __device__ __forceinline__ void load(const float *cum, const float *dl, int tb, int L, int t) {
+        const int r = min(t, L - 1);
+        c = cum[tb + r];
+        d = t < L ? dl[tb + r] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) g[j] = cum[tb + min(32 * j + 31, L - 1)];
+    }
+};
+
 // fp16 copy of a state row (dstate row n: its 64 headdim values) into the M3 operand tile
 __device__ __forceinline__ void store_state_row(uint8_t *sH, int n, const float (&st)[kP]) {
 #pragma unroll
@@ -216,12 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     uint8_t *sXW = smem + OFF_XW, *sH = smem + OFF_H;
-    float *sF = reinterpret_cast<float *>(smem + OFF_F);
-    float *sCc = reinterpret_cast<float *>(smem + OFF_CD);
-    float *sDl = sCc + 128;
+    float *sFCD = reinterpret_cast<float *>(smem + OFF_F);
     float *sE = reinterpret_cast<float *>(smem + OFF_E);
     float *sDec = reinterpret_cast<float *>(smem + OFF_DEC);
-    float *sWT = reinterpret_cast<float *>(smem + OFF_WT);
     uint32_t *sTM = reinterpret_cast<uint32_t *>(smem + OFF_TM);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     auto stage_c = [&](int s) { return smem + s * CB_STAGE; };
@@ -389,48 +400,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp;
         const int t = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const float Ah = p.A[h];
         const float Dh = p.D ? p.D[h] : 0.f;
-        const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
+        const float *cum = p.cum + (size_t)h * p.T, *dl = p.delta + (size_t)h * p.T;
         Cursor cur;
         cur.start(p.cu_chunk, first, last);
-        // dt of row t of the next block, loaded a block ahead from a clamped (always valid)
-        // token; rows past the block's end are masked where it is used
-        __nv_bfloat16 dt_next = p.dt[(size_t)min(cur.tb + t, p.T - 1) * p.H + h];
+        // Row t's delta and cumsum, and the cumsum at the end of each 32-row group (clamped to the
+        // block's last row), loaded one block ahead.  Rows past the block's end take delta 0 and
+        // the cumsum of the last row.
+        RowVals nxt;
+        nxt.load(cum, dl, cur.tb, cur.len(), t);
         for (int i = 0; i < nblocks; ++i, cur.next()) {
             const int s = i & 1;
             const uint32_t ph = (i >> 1) & 1;
             const int L = cur.len();
             uint8_t *sXs = stage_x(i);
             const uint32_t colS = s ? COL_S1 : COL_S0;
-            const __nv_bfloat16 dt_cur = dt_next;
-            dt_next = p.dt[(size_t)min(cur.tb + L + t, p.T - 1) * p.H + h];  // blocks of a sequence are contiguous
-            // ---- delta and the in-block cumsum c_t
-            float delta = 0.f, a = 0.f;
-            if (t < L) {
-                delta = fast_delta(__bfloat162float(dt_cur) + bias, p.dt_softplus, p.dt_min, p.dt_max);
-                a = delta * Ah;
+            const RowVals rv = nxt;
+            if (i + 1 < nblocks) {
+                Cursor cn = cur;
+                cn.next();
+                nxt.load(cum, dl, cn.tb, cn.len(), t);
             }
-            float c = a;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float v = __shfl_up_sync(0xffffffffu, c, off);
-                if (lane >= off) c += v;
-            }
-            if (lane == 31) sWT[q] = c;
-            named_bar_sync(BAR_PG, 128);  // also: every warp is done with the previous block's arrays
-            float wt[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) wt[j] = sWT[j];
-            float prefix = 0.f, own = 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (j < q) prefix += wt[j];
-                if (j == q) own = wt[j];
-            }
-            c += prefix;
-            const float c_last = wt[0] + wt[1] + wt[2] + wt[3];
-            sF[t] = __expf(prefix + own - c) * delta;  // column factor of column t
+            const float c = rv.c, delta = rv.d, c_last = rv.g[3];
+            float *sF = sFCD + (i & 1) * 384, *sCc = sF + 128, *sDl = sF + 256;
+            sF[t] = __expf(rv.g[q] - c) * delta;  // column factor of column t (relative to its group's end)
             sCc[t] = c;
             sDl[t] = delta;
             sE[(i % kRing) * 128 + t] = __expf(c);     // carried-state factor of row t (consumer)
@@ -493,14 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Group j of P goes over columns [16j, 16j+16), which hold S groups <= j that this
             // warp has already read.  The loops stay rolled: the four warp roles run different
             // code, and unrolled copies of these bodies overflow the instruction cache.
-            float gend = 0.f;
 #pragma unroll 1
             for (int j = 0; j < q; ++j) {  // groups below the diagonal
                 uint32_t v[32], pk[16];
                 tmem_ld32(tm + lane_base + colS + 32 * j, v);
-                gend += j == 0 ? wt[0] : (j == 1 ? wt[1] : wt[2]);
-                const float R = __expf(c - gend);
-                const float4 *f4 = reinterpret_cast<const float4 *>(sF + 32 * j);
+                const float R = __expf(c - (j == 0 ? rv.g[0] : (j == 1 ? rv.g[1] : rv.g[2])));
+                const float4 *f4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 384 + 32 * j);
                 tmem_ld_wait();
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -514,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             {  // the diagonal group j = q: one exponential per element, the mask by select
                 uint32_t v[32], pk[16];
                 tmem_ld32(tm + lane_base + colS + 32 * q, v);
-                const float4 *c4 = reinterpret_cast<const float4 *>(sCc + 32 * q);
-                const float4 *d4 = reinterpret_cast<const float4 *>(sDl + 32 * q);
+                const float4 *c4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 384 + 128 + 32 * q);
+                const float4 *d4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 384 + 256 + 32 * q);
                 tmem_ld_wait();
 #pragma unroll
                 for (int u4 = 0; u4 < 8; ++u4) {
@@ -678,22 +669,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// B and C (bf16) -> fp16 once per call: every head of a group reads the same
-// tiles, so converting them here instead of in each head's CTA saves the
-// per-CTA conversion work (and its shared-memory traffic) H/G times over.
-__global__ void __launch_bounds__(256) bc_to_f16_kernel(const uint4 *__restrict__ B, const uint4 *__restrict__ C,
-                                                        uint4 *__restrict__ Bh, uint4 *__restrict__ Ch, size_t n16) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
-        Bh[i] = bf16x8_to_f16x8(B[i]);
-        Ch[i] = bf16x8_to_f16x8(C[i]);
+// Per call, before the fused kernel, one CTA per 128 packed tokens [t0, t0 + 128):
+//  - B and C (bf16) -> fp16: every head of a group reads the same tiles, so converting them once
+//    here instead of in each head's CTA saves that work (and its shared-memory traffic) H/G times;
+//  - delta = clamp(softplus(dt + dt_bias)) and the cumsum of delta * A within each block of the
+//    fused kernel (the 128-token pieces of every chunk, starting at the chunk's first token), for
+//    every head, into [H, T] arrays.  A block may start before t0, so each head first sums the
+//    block's tokens before t0.  Lane = head: the dt loads of a warp are one 64-byte row segment,
+//    and every lane walks the same tokens, so the block starts cost no divergence.
+struct PrepParams {
+    int T, H, K;
+    size_t row16;  // 16-byte units per token row of B (and C)
+    const uint4 *B, *C;
+    uint4 *Bh, *Ch;
+    const __nv_bfloat16 *dt;
+    const float *A, *dt_bias;
+    int dt_softplus;
+    float dt_min, dt_max;
+    const int32_t *cu_chunk;
+    float *cum, *delta;
+};
+
+constexpr int kPrepThreads = 128;
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
+    __shared__ float sC[4][32][33], sD[4][32][33];  // per warp: 32 heads x 32 tokens (padded)
+    const int t0 = blockIdx.x * 128;
+    const int n = min(128, p.T - t0);
+    {
+        const size_t base = (size_t)t0 * p.row16, cnt = (size_t)n * p.row16;
+        for (size_t i = threadIdx.x; i < cnt; i += kPrepThreads) {
+            p.Bh[base + i] = bf16x8_to_f16x8(p.B[base + i]);
+            p.Ch[base + i] = bf16x8_to_f16x8(p.C[base + i]);
+        }
+    }
+    // the chunk holding t0: the last k with cu_chunk[k] <= t0
+    int lo = 0, hi = p.K - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.cu_chunk[mid] <= t0) lo = mid;
+        else hi = mid - 1;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cs0 = p.cu_chunk[lo], ce0 = p.cu_chunk[lo + 1];
+    const int bs = cs0 + ((t0 - cs0) / 128) * 128;  // start of the block holding t0
+    for (int hb = warp; hb * 32 < p.H; hb += 4) {
+        const int h = hb * 32 + lane;
+        const bool hv = h < p.H;
+        const float Ah = hv ? p.A[h] : 0.f;
+        const float bias = (hv && p.dt_bias) ? p.dt_bias[h] : 0.f;
+        const __nv_bfloat16 *dth = p.dt + (hv ? h : 0);
+        int k = lo, ce = ce0;
+        int nbs = min(bs + 128, ce);  // the next block start after bs
+        float run = 0.f;
+        // Tokens [ta, ta + m), m <= 32: the dt loads are all issued first, then the running sum
+        // restarts at every block start (at a chunk's end the next chunk starts a block).
+        auto walk = [&](int ta, int m, bool out) {
+            float dv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dv[j] = j < m ? __bfloat162float(dth[(size_t)(ta + j) * p.H]) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j < m) {
+                    if (ta + j == nbs) {
+                        run = 0.f;
+                        if (nbs == ce && k + 1 < p.K) ce = p.cu_chunk[++k + 1];
+                        nbs = min(nbs + 128, ce);
+                    }
+                    const float d = fast_delta(dv[j] + bias, p.dt_softplus, p.dt_min, p.dt_max);
+                    run += d * Ah;
+                    if (out) {
+                        sC[warp][lane][j] = run;
+                        sD[warp][lane][j] = d;
+                    }
+                }
+            }
+        };
+        for (int ta = bs; ta < t0; ta += 32) walk(ta, min(32, t0 - ta), false);
+        for (int seg = 0; seg < n; seg += 32) {
+            const int m = min(32, n - seg);
+            walk(t0 + seg, m, true);
+            __syncwarp();
+            for (int hh = 0; hh < 32; ++hh) {
+                const int h2 = hb * 32 + hh;
+                if (h2 < p.H && lane < m) {
+                    const size_t o = (size_t)h2 * p.T + t0 + seg + lane;
+                    p.cum[o] = sC[warp][hh][lane];
+                    p.delta[o] = sD[warp][hh][lane];
+                }
+            }
+            __syncwarp();
+        }
     }
 }
 
 }  // namespace
 
+static size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
+
 size_t tc_prefill_workspace(const ssd_prefill_args &a) {
     const size_t bc = (size_t)a.total_tokens * a.ngroups * kN * 2;
-    return 2 * ((bc + 255) & ~(size_t)255);
+    const size_t ht = (size_t)a.total_tokens * a.nheads * 4;
+    return 2 * up256(bc) + 2 * up256(ht);
 }
 
 bool tc_prefill_supported(const ssd_prefill_args &a) {
@@ -704,13 +781,32 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
     CUtensorMap mX, mB, mC;
     const uint64_t T = (uint64_t)a.total_tokens;
     const size_t bc = (size_t)a.total_tokens * a.ngroups * kN * 2;
+    const size_t ht = (size_t)a.total_tokens * a.nheads * 4;
     uint8_t *Bh = static_cast<uint8_t *>(workspace);
-    uint8_t *Ch = Bh + ((bc + 255) & ~(size_t)255);
+    uint8_t *Ch = Bh + up256(bc);
+    float *cum = reinterpret_cast<float *>(Ch + up256(bc));
+    float *delta = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(cum) + up256(ht));
     {
-        const size_t n16 = bc / 16;  // kN * 2 bytes per row: a multiple of 16
-        const int blocks = (int)std::min<size_t>((n16 + 255) / 256, 152 * 8);
-        bc_to_f16_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4 *>(a.B), static_cast<const uint4 *>(a.C),
-                                                reinterpret_cast<uint4 *>(Bh), reinterpret_cast<uint4 *>(Ch), n16);
+        PrepParams q;
+        q.T = a.total_tokens;
+        q.H = a.nheads;
+        q.K = a.num_chunks;
+        q.row16 = (size_t)a.ngroups * kN * 2 / 16;  // kN * 2 bytes per group row: a multiple of 16
+        q.B = static_cast<const uint4 *>(a.B);
+        q.C = static_cast<const uint4 *>(a.C);
+        q.Bh = reinterpret_cast<uint4 *>(Bh);
+        q.Ch = reinterpret_cast<uint4 *>(Ch);
+        q.dt = static_cast<const __nv_bfloat16 *>(a.dt);
+        q.A = a.A;
+        q.dt_bias = a.dt_bias;
+        q.dt_softplus = a.dt_softplus;
+        q.dt_min = a.dt_min;
+        q.dt_max = a.dt_max;
+        q.cu_chunk = a.cu_chunk_seqlens;
+        q.cum = cum;
+        q.delta = delta;
+        const unsigned blocks = (unsigned)((a.total_tokens + 127) / 128);
+        prep_kernel<<<blocks, kPrepThreads, 0, s>>>(q);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -744,6 +840,8 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
     p.err = a.err_word;
     p.seq_order = a.seq_order;
     p.wait_limit = a.wait_limit_cycles > 0 ? (long long)a.wait_limit_cycles : 2000000000ll;
+    p.cum = cum;
+    p.delta = delta;
     auto kernel = p.z ? ssd_prefill_tc_kernel<true> : ssd_prefill_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;

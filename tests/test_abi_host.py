@@ -145,10 +145,11 @@ def test_cuda_core_workspace_is_the_documented_formula(lib, T, H, K, P, N):
 
 @pytest.mark.parametrize("T,G", [(1, 1), (777, 8), (65536, 8)])
 def test_tensor_core_workspace_is_the_documented_formula(lib, T, G):
-    """bf16 with headdim 64 and dstate 128: fp16 copies of B and C, 2 up256(2 T G N) bytes."""
+    """bf16 with headdim 64 and dstate 128: fp16 copies of B and C plus delta and its in-block
+    cumsum per head and token, 2 up256(2 T G N) + 2 up256(4 H T) bytes."""
     a = _prefill_args(total_tokens=T, nheads=2 * G, ngroups=G, headdim=64, dstate=128, dtype=B.SSD_BF16)
     assert lib.ssd_prefill_kernel_count(ctypes.byref(a)) == 2
-    assert lib.ssd_prefill_workspace_size(ctypes.byref(a)) == 2 * _up256(2 * T * G * 128)
+    assert lib.ssd_prefill_workspace_size(ctypes.byref(a)) == 2 * _up256(2 * T * G * 128) + 2 * _up256(4 * 2 * G * T)
 
 
 def test_noalloc_refusal_is_decided_on_the_host(lib):
