@@ -212,17 +212,24 @@ typedef struct ssd_prefill_args {
 } ssd_prefill_args;
 
 /* Bytes of device workspace ssd_prefill_varlen needs for these arguments
- * (sizes only are read).  0 on invalid sizes.  With up256 rounding up to a
- * multiple of 256: bf16 with headdim 64 and dstate 128 (the tensor-core
- * kernel) needs the fp16 copies of B and C and, per head and token, delta and
- * its in-block cumsum: 2*up256(2*T*G*N) + 2*up256(4*H*T) bytes; every
+ * (sizes only are read) on the current device.  0 on invalid sizes.  With
+ * up256 rounding up to a multiple of 256: bf16 with headdim 64 and dstate 128
+ * (the tensor-core kernel) needs the fp16 copies of B and C and, per head and
+ * token, delta and its in-block cumsum: 2*up256(2*T*G*N) + 2*up256(4*H*T)
+ * bytes.  When S*H is below half the device's SM count, each sequence is cut
+ * into k segments of whole 128-token blocks (k = min(SMs / (S*H), T / S / 256,
+ * 8), at least 1) that separate CTAs run, and k > 1 adds
+ * up256(4*S*(k-1)*H*P*N) + up256(4*S*(k-1)*H) bytes for the state and decay
+ * at the end of each segment but the last.  Every
  * other case (the CUDA-core path) needs up256(4*H*T) + up256(8*H*T) +
  * 2*up256(4*K*H*P*N) for delta, the fp64 cumsum, the chunk states and the
  * states entering each chunk. */
 SSD_API size_t ssd_prefill_workspace_size(const ssd_prefill_args *args);
 
 /* Number of CUDA kernels one ssd_prefill_varlen call with these arguments
- * launches (0 for an empty call, -1 on invalid sizes).  Host only. */
+ * launches on the current device (0 for an empty call, -1 on invalid sizes):
+ * 2 for the tensor-core path (3 when it cuts sequences into segments), 4 for
+ * the CUDA-core path.  Host only. */
 SSD_API int32_t ssd_prefill_kernel_count(const ssd_prefill_args *args);
 
 /*

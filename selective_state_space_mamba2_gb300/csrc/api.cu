@@ -63,7 +63,7 @@ extern "C" size_t ssd_prefill_workspace_size(const ssd_prefill_args *a) {
 extern "C" int32_t ssd_prefill_kernel_count(const ssd_prefill_args *a) {
     if (check_prefill(a) != SSD_OK) return -1;
     if (a->total_tokens == 0) return 0;
-    return ssd::tc_prefill_supported(*a) ? 2 : 4;
+    return ssd::tc_prefill_supported(*a) ? (ssd::tc_prefill_segments(*a) > 1 ? 3 : 2) : 4;
 }
 
 extern "C" ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *a, void *workspace,

@@ -86,6 +86,7 @@ cudaError_t simt_prefill_launch(const ssd_prefill_args &a, const PrefillWorkspac
 bool simt_prefill_supported(const ssd_prefill_args &a);
 
 bool tc_prefill_supported(const ssd_prefill_args &a);
+int tc_prefill_segments(const ssd_prefill_args &a);
 size_t tc_prefill_workspace(const ssd_prefill_args &a);
 cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s);
 

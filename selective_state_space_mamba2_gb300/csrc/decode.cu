@@ -19,10 +19,20 @@ namespace ssd {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kTokBatch = 8;  // tokens whose inputs are staged together
+
+// Shared memory of one CTA: per staged token, x and y [P], B and C [N] and delta.
+__host__ __device__ inline size_t decode_smem_bytes(int P, int N) {
+    return (size_t)kTokBatch * (2 * P + 2 * N + 1) * sizeof(float);
+}
 
 // At least 4 resident CTAs per SM (at most 64 registers) while the state takes up to 32
 // floats per thread: the kernel is HBM-bound, and occupancy is what keeps enough state loads
 // in flight.  The 64-float case keeps its registers (2 CTAs per SM).
+//
+// The tokens of a request are taken in batches of up to kTokBatch: their x, B, C and delta are
+// loaded together (one memory latency per batch, not per token), and each token reduces into its
+// own y row, so the tokens of a batch follow each other with no barrier in between.
 template <typename Tin, int VPT, bool kGate>
 __global__ void __launch_bounds__(kThreads, VPT >= 16 ? 2 : 4)
     ssm_decode_kernel(const ssm_decode_args a) {
@@ -46,7 +56,12 @@ __global__ void __launch_bounds__(kThreads, VPT >= 16 ? 2 : 4)
         return;
     }
 
-    __shared__ float sx[256], sB[256], sC[256], sy[256];
+    extern __shared__ __align__(16) float dsm[];
+    float *sx = dsm;                   // [kTokBatch][P]
+    float *sy = sx + kTokBatch * P;    // [kTokBatch][P]
+    float *sB = sy + kTokBatch * P;    // [kTokBatch][N]
+    float *sC = sB + kTokBatch * N;    // [kTokBatch][N]
+    float *sD = sC + kTokBatch * N;    // [kTokBatch] delta
 
     const int PN = P * N;
     const int nvec = PN >> 2;  // float4 chunks; N % 4 == 0
@@ -74,53 +89,67 @@ __global__ void __launch_bounds__(kThreads, VPT >= 16 ? 2 : 4)
     const Tin *z = static_cast<const Tin *>(a.z);  // output gate or NULL
     Tin *y = static_cast<Tin *>(a.y);
 
-    for (int k = 0; k < tpr; ++k) {
-        const size_t row = (size_t)r * tpr + k;
-        __syncthreads();  // the previous token's readers of sx/sy are done
-        for (int j = tid; j < P; j += kThreads) {
-            sx[j] = ldg_f32(x + (row * H + h) * P + j);
-            sy[j] = 0.f;
+    for (int k0 = 0; k0 < tpr; k0 += kTokBatch) {
+        const int kb = min(kTokBatch, tpr - k0);
+        __syncthreads();  // the previous batch's readers of the staging arrays are done
+        for (int j = tid; j < kb * P; j += kThreads) {
+            const int kk = j / P, pp = j - kk * P;
+            const size_t row = (size_t)r * tpr + k0 + kk;
+            sx[kk * P + pp] = ldg_f32(x + (row * H + h) * P + pp);
+            sy[kk * P + pp] = 0.f;
         }
-        for (int j = tid; j < N; j += kThreads) {
-            sB[j] = ldg_f32(Bp + (row * a.ngroups + g) * N + j);
-            sC[j] = ldg_f32(Cp + (row * a.ngroups + g) * N + j);
+        for (int j = tid; j < kb * N; j += kThreads) {
+            const int kk = j / N, nn = j - kk * N;
+            const size_t row = (size_t)r * tpr + k0 + kk;
+            sB[kk * N + nn] = ldg_f32(Bp + (row * a.ngroups + g) * N + nn);
+            sC[kk * N + nn] = ldg_f32(Cp + (row * a.ngroups + g) * N + nn);
         }
-        __syncthreads();
-        const float delta = step_delta(ldg_f32(dtp + row * H + h) + bias, a.dt_softplus, a.dt_min, a.dt_max);
-        const float decay = __expf(delta * A);
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            const int e = tid + i * kThreads;
-            float part = 0.f;
-            int p = 0;
-            if (e < nvec) {
-                p = e / quads;
-                const int n = (e - p * quads) << 2;
-                const float dx = delta * sx[p];
-                s[i].x = fmaf(decay, s[i].x, dx * sB[n + 0]);
-                s[i].y = fmaf(decay, s[i].y, dx * sB[n + 1]);
-                s[i].z = fmaf(decay, s[i].z, dx * sB[n + 2]);
-                s[i].w = fmaf(decay, s[i].w, dx * sB[n + 3]);
-                part = s[i].x * sC[n] + s[i].y * sC[n + 1] + s[i].z * sC[n + 2] + s[i].w * sC[n + 3];
-            }
-            // segmented reduction over the lanes that share p
-            for (int off = seg >> 1; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-            if (e < nvec && (threadIdx.x & (seg - 1)) == 0) atomicAdd(&sy[p], part);
+        if (tid < kb) {
+            const size_t row = (size_t)r * tpr + k0 + tid;
+            sD[tid] = step_delta(ldg_f32(dtp + row * H + h) + bias, a.dt_softplus, a.dt_min, a.dt_max);
         }
         __syncthreads();
-        for (int j = tid; j < P; j += kThreads) {
-            const size_t o = (row * H + h) * P + j;
-            const float v = sy[j] + Dh * sx[j];
-            y[o] = from_f32<Tin>(kGate ? silu_gate(v, ldg_f32(z + o)) : v);
-        }
-        const int32_t ws = row_slots[k];
-        if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr)) {
-            float4 *dst = reinterpret_cast<float4 *>(a.state_cache + (size_t)ws * H * PN + head_off);
+        for (int kk = 0; kk < kb; ++kk) {
+            const float delta = sD[kk];
+            const float decay = __expf(delta * A);
+            const float *xk = sx + kk * P, *Bk = sB + kk * N, *Ck = sC + kk * N;
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int e = tid + i * kThreads;
-                if (e < nvec) dst[e] = s[i];
+                float part = 0.f;
+                int p = 0;
+                if (e < nvec) {
+                    p = e / quads;
+                    const int n = (e - p * quads) << 2;
+                    const float dx = delta * xk[p];
+                    const float4 b4 = *reinterpret_cast<const float4 *>(Bk + n);
+                    const float4 c4 = *reinterpret_cast<const float4 *>(Ck + n);
+                    s[i].x = fmaf(decay, s[i].x, dx * b4.x);
+                    s[i].y = fmaf(decay, s[i].y, dx * b4.y);
+                    s[i].z = fmaf(decay, s[i].z, dx * b4.z);
+                    s[i].w = fmaf(decay, s[i].w, dx * b4.w);
+                    part = s[i].x * c4.x + s[i].y * c4.y + s[i].z * c4.z + s[i].w * c4.w;
+                }
+                // segmented reduction over the lanes that share p
+                for (int off = seg >> 1; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+                if (e < nvec && (threadIdx.x & (seg - 1)) == 0) atomicAdd(&sy[kk * P + p], part);
             }
+            const int32_t ws = row_slots[k0 + kk];
+            if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr)) {
+                float4 *dst = reinterpret_cast<float4 *>(a.state_cache + (size_t)ws * H * PN + head_off);
+#pragma unroll
+                for (int i = 0; i < VPT; ++i) {
+                    const int e = tid + i * kThreads;
+                    if (e < nvec) dst[e] = s[i];
+                }
+            }
+        }
+        __syncthreads();
+        for (int j = tid; j < kb * P; j += kThreads) {
+            const int kk = j / P, pp = j - kk * P;
+            const size_t o = (((size_t)r * tpr + k0 + kk) * H + h) * P + pp;
+            const float v = sy[j] + Dh * sx[j];
+            y[o] = from_f32<Tin>(kGate ? silu_gate(v, ldg_f32(z + o)) : v);
         }
     }
 }
@@ -130,18 +159,19 @@ cudaError_t launch_typed(const ssm_decode_args &a, cudaStream_t st) {
     const int nvec = a.headdim * a.dstate / 4;
     const int vpt = (nvec + kThreads - 1) / kThreads;
     dim3 grid(a.batch, a.nheads);
+    const size_t sm = decode_smem_bytes(a.headdim, a.dstate);
     if (a.z) {  // gated instances: y * silu(z)
-        if (vpt <= 1) ssm_decode_kernel<Tin, 1, true><<<grid, kThreads, 0, st>>>(a);
-        else if (vpt <= 2) ssm_decode_kernel<Tin, 2, true><<<grid, kThreads, 0, st>>>(a);
-        else if (vpt <= 4) ssm_decode_kernel<Tin, 4, true><<<grid, kThreads, 0, st>>>(a);
-        else if (vpt <= 8) ssm_decode_kernel<Tin, 8, true><<<grid, kThreads, 0, st>>>(a);
-        else ssm_decode_kernel<Tin, 16, true><<<grid, kThreads, 0, st>>>(a);
+        if (vpt <= 1) ssm_decode_kernel<Tin, 1, true><<<grid, kThreads, sm, st>>>(a);
+        else if (vpt <= 2) ssm_decode_kernel<Tin, 2, true><<<grid, kThreads, sm, st>>>(a);
+        else if (vpt <= 4) ssm_decode_kernel<Tin, 4, true><<<grid, kThreads, sm, st>>>(a);
+        else if (vpt <= 8) ssm_decode_kernel<Tin, 8, true><<<grid, kThreads, sm, st>>>(a);
+        else ssm_decode_kernel<Tin, 16, true><<<grid, kThreads, sm, st>>>(a);
     } else {
-        if (vpt <= 1) ssm_decode_kernel<Tin, 1, false><<<grid, kThreads, 0, st>>>(a);
-        else if (vpt <= 2) ssm_decode_kernel<Tin, 2, false><<<grid, kThreads, 0, st>>>(a);
-        else if (vpt <= 4) ssm_decode_kernel<Tin, 4, false><<<grid, kThreads, 0, st>>>(a);
-        else if (vpt <= 8) ssm_decode_kernel<Tin, 8, false><<<grid, kThreads, 0, st>>>(a);
-        else ssm_decode_kernel<Tin, 16, false><<<grid, kThreads, 0, st>>>(a);
+        if (vpt <= 1) ssm_decode_kernel<Tin, 1, false><<<grid, kThreads, sm, st>>>(a);
+        else if (vpt <= 2) ssm_decode_kernel<Tin, 2, false><<<grid, kThreads, sm, st>>>(a);
+        else if (vpt <= 4) ssm_decode_kernel<Tin, 4, false><<<grid, kThreads, sm, st>>>(a);
+        else if (vpt <= 8) ssm_decode_kernel<Tin, 8, false><<<grid, kThreads, sm, st>>>(a);
+        else ssm_decode_kernel<Tin, 16, false><<<grid, kThreads, sm, st>>>(a);
     }
     return cudaGetLastError();
 }

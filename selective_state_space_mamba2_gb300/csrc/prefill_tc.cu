@@ -65,6 +65,9 @@ struct TcParams {
     long long wait_limit;  // cycles a device-side wait may take before the CTA gives up
     const float *cum;      // [H, T] in-block inclusive cumsum of delta * A (written by prep_kernel)
     const float *delta;    // [H, T] delta (written by prep_kernel)
+    int nseg;              // segments each sequence is cut into (1: none)
+    float *seg_state;      // [S, nseg - 1, H, P, N]: state at the end of segments 0 .. nseg - 2
+    float *seg_decay;      // [S, nseg - 1, H]: for segments 1 .. nseg - 2, the product of their decays
 };
 
 namespace {
@@ -93,7 +96,8 @@ constexpr uint32_t OFF_F = OFF_H + 16384;    // column factors, c_t and delta_t:
 constexpr uint32_t OFF_E = OFF_F + 3072;     // exp(c_t) per block, ring of 4 [4][128]
 constexpr uint32_t OFF_DEC = OFF_E + 2048;   // exp(c_L) per block, ring of 4
 constexpr uint32_t OFF_TM = OFF_DEC + 16;    // TMEM base address
-constexpr uint32_t OFF_BAR = OFF_TM + 16;    // mbarriers
+constexpr uint32_t OFF_INFO = OFF_TM + 16;   // the CTA's part of its sequence [4]
+constexpr uint32_t OFF_BAR = OFF_INFO + 16;  // mbarriers
 constexpr uint32_t kSmemBytes = OFF_BAR + 24 * 8;
 constexpr int kRing = 4;
 
@@ -137,20 +141,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, long l
     return ok;
 }
 
-// Walks the blocks of one sequence: chunks [first, last], each cut into
-// blocks of at most kL tokens that never cross a chunk end.  The end of the
+// Walks the blocks of one sequence (or of one segment of it, from any block
+// start): chunks up to last, each cut into blocks of at most kL tokens that
+// never cross a chunk end.  The end of the
 // following chunk is loaded one chunk ahead (from a clamped index, so the
 // load is unconditional), so moving to the next chunk never waits on memory.
 struct Cursor {
     const int32_t *cu_chunk;
     int k, last, tb, ce, ce_next;
-    __device__ void start(const int32_t *cc, int first, int last_) {
+    // from block start tb inside chunk k
+    __device__ void start_at(const int32_t *cc, int k_, int tb_, int last_) {
         cu_chunk = cc;
-        k = first;
+        k = k_;
         last = last_;
-        tb = cc[first];
-        ce = cc[first + 1];
-        ce_next = cc[min(first + 2, last_ + 1)];
+        tb = tb_;
+        ce = cc[k_ + 1];
+        ce_next = cc[min(k_ + 2, last_ + 1)];
     }
     __device__ int len() const { return min(kL, ce - tb); }
     __device__ bool ends_chunk() const { return tb + len() == ce; }
@@ -191,40 +197,89 @@ __device__ __forceinline__ void store_state_row(uint8_t *sH, int n, const float 
 }
 
 // kGate: y is multiplied by silu(z) (a separate instance, so the ungated kernel keeps its
-// registers for the rest of the epilogue)
-template <bool kGate>
+// registers for the rest of the epilogue).
+// kState: the segment pass.  When a sequence is cut into nseg segments of whole blocks (too few
+// sequences and heads to fill the GPU), this instance runs first, one CTA per (sequence, segment
+// 0 .. nseg - 2, head): x, B, w x, M4 and the state update only, from the initial state for
+// segment 0 and from zero for the others.  It writes each segment's end state and, for segments
+// 1 .., the product of its blocks' decays.  The full instance then runs one CTA per (sequence,
+// segment, head) and starts segment j >= 1 from the state those give at its first token.
+template <bool kGate, bool kState>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slot_r = blockIdx.x / p.H;
-    const int h = blockIdx.x - slot_r * p.H;
+    const int nsg = kState ? p.nseg - 1 : p.nseg;  // segments with a CTA in this launch
+    const int slot_r = blockIdx.x / (p.H * nsg);
+    const int jh = blockIdx.x - slot_r * p.H * nsg;
+    const int j = jh / p.H;  // segment
+    const int h = jh - j * p.H;
     const int r = p.seq_order ? p.seq_order[slot_r] : slot_r;
     if (r < 0 || r >= p.S) {
-        if (tid == 0 && h == 0) report(p.err, SSD_DEVERR_METADATA);
+        if (tid == 0 && h == 0 && j == 0) report(p.err, SSD_DEVERR_METADATA);
         return;
     }
     const int g = h / (p.H / p.G);
 
-    // ---- the sequence's chunk range, validated before anything is set up
+    // ---- the sequence's chunk range, validated, and this CTA's part of it: blocks [b0, b1) of
+    //      the sequence's nb, b0 = j nb / nseg.  Warp 8 works it out, 32 chunks per step.
     const int first = r > 0 ? p.last_chunk[r - 1] + 1 : 0;
     const int last = p.last_chunk[r];
-    if (last < first) return;  // no new tokens
-    int nblocks = 0;
-    {
-        bool bad = first < 0 || last >= p.K || p.cu_chunk[first] != p.cu_seqlens[r] ||
-                   p.cu_chunk[last + 1] != p.cu_seqlens[r + 1];
-        for (int k = first; !bad && k <= last; ++k) {
-            const int a = p.cu_chunk[k], b = p.cu_chunk[k + 1];
-            if (a < 0 || b <= a || b > p.T) bad = true;
-            else nblocks += (b - a + kL - 1) / kL;
+    int *sInfo = reinterpret_cast<int *>(smem + OFF_INFO);
+    if (warp == kProducerWarp) {
+        bool bad = last >= first && (first < 0 || last >= p.K || p.cu_chunk[first] != p.cu_seqlens[r] ||
+                                     p.cu_chunk[last + 1] != p.cu_seqlens[r + 1]);
+        int total = 0;
+        if (last >= first && !bad) {
+            for (int k0 = first; k0 <= last; k0 += 32) {
+                const int k = k0 + lane;
+                int nb = 0;
+                if (k <= last) {
+                    const int a = p.cu_chunk[k], b = p.cu_chunk[k + 1];
+                    if (a < 0 || b <= a || b > p.T) bad = true;
+                    else nb = (b - a + kL - 1) / kL;
+                }
+                total += __reduce_add_sync(0xffffffffu, nb);
+            }
+            bad = __any_sync(0xffffffffu, bad);
         }
-        if (bad) {
-            if (tid == 0 && h == 0) report(p.err, SSD_DEVERR_METADATA);
-            return;
+        const int b0 = (int)((long long)j * total / p.nseg), b1 = (int)((long long)(j + 1) * total / p.nseg);
+        int seg_k = first, seg_tb = 0;
+        if (!bad && b1 > b0) {
+            seg_tb = p.cu_chunk[first];
+            int before = 0;  // blocks in the chunks of earlier steps
+            for (int k0 = first; b0 > 0 && k0 <= last; k0 += 32) {
+                const int k = k0 + lane;
+                const int nb = k <= last ? (p.cu_chunk[k + 1] - p.cu_chunk[k] + kL - 1) / kL : 0;
+                int incl = nb;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += v;
+                }
+                const unsigned m = __ballot_sync(0xffffffffu, nb > 0 && before + incl - nb <= b0 && b0 < before + incl);
+                if (m) {
+                    const int src = __ffs(m) - 1;
+                    seg_k = __shfl_sync(0xffffffffu, k, src);
+                    seg_tb = p.cu_chunk[seg_k] + (b0 - before - __shfl_sync(0xffffffffu, incl - nb, src)) * kL;
+                    break;
+                }
+                before += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        if (lane == 0) {
+            sInfo[0] = seg_k;
+            sInfo[1] = seg_tb;
+            sInfo[2] = bad ? 0 : b1 - b0;
+            sInfo[3] = bad;
+            if (bad && h == 0 && j == 0) report(p.err, SSD_DEVERR_METADATA);
         }
     }
+    __syncthreads();
+    const int seg_k = sInfo[0], seg_tb = sInfo[1], nblocks = sInfo[2];
+    if (sInfo[3]) return;
+    if (!kState && nblocks == 0) return;  // no new tokens (or none in this segment)
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
         if (tid == 0) report(p.err, SSD_DEVERR_INTERNAL);
         return;
@@ -267,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The idle lanes check, for one head of each sequence, that seq_order names this
             // sequence exactly once (with every entry in range, a permutation then follows): a
             // repeated entry would run one sequence twice and leave another's y unwritten.
-            if (h == 0 && p.seq_order) {
+            if (!kState && h == 0 && j == 0 && p.seq_order) {
                 int cnt = 0;
                 for (int i = lane - 1; i < p.S; i += 31) cnt += p.seq_order[i] == r;
                 cnt = __reduce_add_sync(0xfffffffeu, cnt);
@@ -277,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Two rings, each refilled as soon as its slot frees: C/B tiles once M3 of the
             // block two back is done, x tiles once y of the block three back is out.
             Cursor ccb, cx;
-            ccb.start(p.cu_chunk, first, last);
-            cx.start(p.cu_chunk, first, last);
+            ccb.start_at(p.cu_chunk, seg_k, seg_tb, last);
+            cx.start_at(p.cu_chunk, seg_k, seg_tb, last);
             int ncb = 0, nx = 0;
             long long t_prog = clock64();
             while (ncb < nblocks || nx < nblocks) {
@@ -287,9 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int s = ncb & 1;
                     if (ncb < kCbStages || mbar_test(&bar[EMPTY_CB0 + s], ((ncb >> 1) - 1) & 1)) {
                         uint64_t *full = &bar[FULL_CB0 + s];
-                        mbar_arrive_expect_tx(full, CB_STAGE);
-                        tma_load_3d(stage_c(s), &tmC, 0, g, ccb.tb, full);
-                        tma_load_3d(stage_c(s) + 16384, &tmC, 64, g, ccb.tb, full);
+                        mbar_arrive_expect_tx(full, kState ? CB_STAGE / 2 : CB_STAGE);  // the segment pass needs no C
+                        if (!kState) {
+                            tma_load_3d(stage_c(s), &tmC, 0, g, ccb.tb, full);
+                            tma_load_3d(stage_c(s) + 16384, &tmC, 64, g, ccb.tb, full);
+                        }
                         tma_load_3d(stage_b(s), &tmB, 0, g, ccb.tb, full);
                         tma_load_3d(stage_b(s) + 16384, &tmB, 64, g, ccb.tb, full);
                         ccb.next();
@@ -327,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ MMA issue -------
         if (lane == 0) {
+            int nblocks_mma = nblocks;
             constexpr uint32_t kIdS = idesc_f16(128, 128, 0, 0);
             constexpr uint32_t kIdY = idesc_f16(128, 64, 0, 1);
             constexpr uint32_t kIdD = idesc_f16(128, 64, 1, 1);
@@ -350,14 +408,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&bar[S_RDY0 + sb]);
             };
-            bool ok = mbar_wait(&bar[FULL_CB0], 0, p.wait_limit);
-            if (ok) {
+            bool ok = true;
+            if (kState) {
+                // the segment pass: M4 only, per block
+                for (int i = 0; ok && i < nblocks; ++i) {
+                    const int s = i & 1;
+                    if (!(ok = mbar_wait(&bar[OPS_W], i & 1, p.wait_limit)) || !(ok = mbar_wait(&bar[DS_FREE], i & 1, p.wait_limit)) ||
+                        !(ok = mbar_wait(&bar[FULL_CB0 + s], (i >> 1) & 1, p.wait_limit)))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_ss(tm + COL_DS, desc_at(s ? dBm1 : dBm0, 2048 * k), desc_at(dXW, 2048 * k), kIdD, k > 0);
+                    mma_commit(&bar[ACC_DS]);
+                    mma_commit(&bar[EMPTY_CB0 + s]);
+                }
+                nblocks_mma = 0;  // the loop below is the full pass
+            } else if ((ok = mbar_wait(&bar[FULL_CB0], 0, p.wait_limit))) {
                 tc_fence_after();
                 issue_m1(0);
             }
             // Per block, in this order: M4 (the state update waits on it), M3, M2 (y), then M1 of
             // the next block, whose S is needed only after the next block's scan and w x.
-            for (int i = 0; ok && i < nblocks; ++i) {
+            for (int i = 0; ok && i < nblocks_mma; ++i) {
                 const int s = i & 1, xs = i % kXStages;
                 const uint64_t dCs = s ? dC1 : dC0, dBms = s ? dBm1 : dBm0;
                 const uint64_t dXs = xs == 0 ? dX0 : (xs == 1 ? dX1 : dX2);
@@ -385,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 8; ++k)
                     mma_ts(tm + COL_Y1, tm + (s ? COL_S1 : COL_S0) + 8 * k, desc_at(dXs, 2048 * k), kIdY, k > 0);
                 mma_commit(&bar[ACC_Y]);
-                if (i + 1 < nblocks) {
+                if (i + 1 < nblocks_mma) {
                     if (!(ok = mbar_wait(&bar[FULL_CB0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1, p.wait_limit))) break;
                     tc_fence_after();
                     issue_m1(i + 1);
@@ -403,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float Dh = p.D ? p.D[h] : 0.f;
         const float *cum = p.cum + (size_t)h * p.T, *dl = p.delta + (size_t)h * p.T;
         Cursor cur;
-        cur.start(p.cu_chunk, first, last);
+        cur.start_at(p.cu_chunk, seg_k, seg_tb, last);
         // Row t's delta and cumsum, and the cumsum at the end of each 32-row group (clamped to the
         // block's last row), loaded one block ahead.  Rows past the block's end take delta 0 and
         // the cumsum of the last row.
@@ -422,11 +495,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nxt.load(cum, dl, cn.tb, cn.len(), t);
             }
             const float c = rv.c, delta = rv.d, c_last = rv.g[3];
-            float *sF = sFCD + (i & 1) * 384, *sCc = sF + 128, *sDl = sF + 256;
-            sF[t] = __expf(rv.g[q] - c) * delta;  // column factor of column t (relative to its group's end)
-            sCc[t] = c;
-            sDl[t] = delta;
-            sE[(i % kRing) * 128 + t] = __expf(c);     // carried-state factor of row t (consumer)
+            if constexpr (!kState) {
+                float *sF = sFCD + (i & 1) * 384, *sCc = sF + 128, *sDl = sF + 256;
+                sF[t] = __expf(rv.g[q] - c) * delta;  // column factor of column t (relative to its group's end)
+                sCc[t] = c;
+                sDl[t] = delta;
+                sE[(i % kRing) * 128 + t] = __expf(c);  // carried-state factor of row t (consumer)
+            }
             if (t == 0) sDec[i % kRing] = __expf(c_last);
             // w_t as fp16x2, for w x computed as an fp16 product of the (exactly) converted x
             const uint32_t w2 = pack_f16_sat(__expf(c_last - c) * delta, __expf(c_last - c) * delta);
@@ -449,7 +524,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       hmul2_u32(xh.w, w2));
                 if (!live) xh = xw = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
-                *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = xh;
+                if (!kState) *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = xh;
+            }
+            if constexpr (kState) {
+                // the segment pass: B's rows past a short block's end are cleared for M4 (no M1 reads
+                // the stage here); the x slot is free once w x is written
+                if (L < kL && !live) {
+                    uint8_t *sB = stage_b(s);
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        *reinterpret_cast<uint4 *>(sB + sw128_offset(t, cc)) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(sB + 16384 + sw128_offset(t, cc)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bar[OPS_W]);
+                    mbar_arrive(&bar[EMPTY_X0 + i % kXStages]);
+                }
+                continue;
             }
             bool s_ready = false;
             if (L < kL) {
@@ -544,7 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const size_t HPN = (size_t)p.H * kP * kN;
         float st[kP];  // state h[p][n = t]
-        {
+        // segment outputs of this sequence and head: [segment][P][N] with a stride of H P N
+        const size_t seg0 = ((size_t)r * (p.nseg - 1) * p.H + h) * kP * kN + t;
+        if (j == 0) {  // the sequence's initial state
             const int32_t is = p.init_slot ? p.init_slot[r] : p.null_id;
             if (slot_usable(is, p.null_id, p.num_slots, (t == 0) ? p.err : nullptr)) {
                 const float *src = p.cache + (size_t)is * HPN + (size_t)h * kP * kN + t;
@@ -554,7 +650,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < kP; ++e) st[e] = 0.f;
             }
+        } else if (kState) {  // later segments of the segment pass start from zero
+#pragma unroll
+            for (int e = 0; e < kP; ++e) st[e] = 0.f;
+        } else {  // the state at this segment's first token: segment 0's end, carried through 1 .. j-1
+#pragma unroll
+            for (int e = 0; e < kP; ++e) st[e] = p.seg_state[seg0 + (size_t)e * kN];
+            for (int jj = 1; jj < j; ++jj) {
+                const float d = p.seg_decay[((size_t)r * (p.nseg - 1) + jj) * p.H + h];
+                const float *src = p.seg_state + seg0 + (size_t)jj * HPN;
+#pragma unroll
+                for (int e = 0; e < kP; ++e) st[e] = fmaf(d, st[e], src[(size_t)e * kN]);
+            }
         }
+        if constexpr (kState) {
+            // the segment pass: the state through the segment's blocks, then its end state and
+            // the product of its decays
+            if (lane == 0) mbar_arrive(&bar[DS_FREE]);
+            float dprod = 1.f;
+            for (int i = 0; i < nblocks; ++i) {
+                bool ok = warp_wait(&bar[ACC_DS], i & 1, p.wait_limit);
+                if (!named_bar_and(BAR_CG, 128, ok)) {
+                    if (t == 0) report(p.err, SSD_DEVERR_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const float decay = sDec[i % kRing];
+                uint32_t d[64];
+                tmem_ld64(tm + lane_base + COL_DS, d);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 64; ++e) st[e] = fmaf(decay, st[e], __uint_as_float(d[e]));
+                dprod *= decay;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[DS_FREE]);
+            }
+            float *dst = p.seg_state + seg0 + (size_t)j * HPN;
+#pragma unroll
+            for (int e = 0; e < kP; ++e) dst[(size_t)e * kN] = st[e];
+            if (t == 0) p.seg_decay[((size_t)r * (p.nseg - 1) + j) * p.H + h] = dprod;
+        } else {
         store_state_row(sH, t, st);
         fence_proxy_async_smem();
         __syncwarp();
@@ -564,9 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bar[Y1_FREE]);
         }
         Cursor cur;
-        cur.start(p.cu_chunk, first, last);
+        cur.start_at(p.cu_chunk, seg_k, seg_tb, last);
         // cache slot of the current chunk's end state, loaded a chunk ahead of its use
-        int32_t cs = p.chunk_slot ? p.chunk_slot[first] : p.null_id;
+        int32_t cs = p.chunk_slot ? p.chunk_slot[seg_k] : p.null_id;
         for (int i = 0; i < nblocks; ++i, cur.next()) {
             const int s = i & 1;
             const int tb = cur.tb, L = cur.len();
@@ -660,6 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[EMPTY_X0 + i % kXStages]);
         }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -669,16 +806,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Per call, before the fused kernel, one CTA per 128 packed tokens [t0, t0 + 128):
+// Per call, before the fused kernel:
 //  - B and C (bf16) -> fp16: every head of a group reads the same tiles, so converting them once
-//    here instead of in each head's CTA saves that work (and its shared-memory traffic) H/G times;
+//    here instead of in each head's CTA saves that work (and its shared-memory traffic) H/G times.
 //  - delta = clamp(softplus(dt + dt_bias)) and the cumsum of delta * A within each block of the
 //    fused kernel (the 128-token pieces of every chunk, starting at the chunk's first token), for
-//    every head, into [H, T] arrays.  A block may start before t0, so each head first sums the
-//    block's tokens before t0.  Lane = head: the dt loads of a warp are one 64-byte row segment,
-//    and every lane walks the same tokens, so the block starts cost no divergence.
+//    every head, into [H, T] arrays.
+// The scan CTAs come first, one per (chunk, piece, 32 heads): piece m of chunk k is the block
+// starting at token cu_chunk[k] + 128 m (pieces m + mpc, m + 2 mpc, ... too, for a chunk longer
+// than mpc pieces).  Its four warps take 32 tokens each, lane = head (so the dt loads of a warp
+// are 64-byte row segments); each scans its 32 tokens on its own, and a warp adds the totals of
+// the warps before it.  The conversion CTAs follow, grid-stride.
 struct PrepParams {
     int T, H, K;
+    int mpc;       // pieces per chunk with a CTA of their own (chunk_size / 128, at least 1)
+    int nscan;     // scan CTAs, K * mpc * ceil(H / 32); the rest convert B and C
     size_t row16;  // 16-byte units per token row of B (and C)
     const uint4 *B, *C;
     uint4 *Bh, *Ch;
@@ -690,76 +832,82 @@ struct PrepParams {
     float *cum, *delta;
 };
 
-constexpr int kPrepThreads = 128;
+constexpr int kPrepThreads = 128;  // 4 warps
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
-    __shared__ float sC[4][32][33], sD[4][32][33];  // per warp: 32 heads x 32 tokens (padded)
-    const int t0 = blockIdx.x * 128;
-    const int n = min(128, p.T - t0);
-    {
-        const size_t base = (size_t)t0 * p.row16, cnt = (size_t)n * p.row16;
-        for (size_t i = threadIdx.x; i < cnt; i += kPrepThreads) {
-            p.Bh[base + i] = bf16x8_to_f16x8(p.B[base + i]);
-            p.Ch[base + i] = bf16x8_to_f16x8(p.C[base + i]);
+    __shared__ float sC[32][129], sD[32][129];  // one block's outputs: 32 heads x 128 tokens (padded)
+    __shared__ float sTail[4][32];              // per warp and head: the sum over its 32 tokens
+    if ((int)blockIdx.x >= p.nscan) {
+        // B and C -> fp16, grid-stride over 16-byte units, four of each in flight per thread
+        const size_t cnt = (size_t)p.T * p.row16;
+        const size_t stride = (size_t)(gridDim.x - p.nscan) * kPrepThreads;
+        size_t i = (size_t)(blockIdx.x - p.nscan) * kPrepThreads + threadIdx.x;
+        for (; i + 3 * stride < cnt; i += 4 * stride) {
+            uint4 b[4], c[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                b[u] = p.B[i + u * stride];
+                c[u] = p.C[i + u * stride];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                p.Bh[i + u * stride] = bf16x8_to_f16x8(b[u]);
+                p.Ch[i + u * stride] = bf16x8_to_f16x8(c[u]);
+            }
         }
+        for (; i < cnt; i += stride) {
+            p.Bh[i] = bf16x8_to_f16x8(p.B[i]);
+            p.Ch[i] = bf16x8_to_f16x8(p.C[i]);
+        }
+        return;
     }
-    // the chunk holding t0: the last k with cu_chunk[k] <= t0
-    int lo = 0, hi = p.K - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.cu_chunk[mid] <= t0) lo = mid;
-        else hi = mid - 1;
-    }
+    const int nhb = (p.H + 31) / 32;
+    const int hb = blockIdx.x % nhb;
+    const int km = blockIdx.x / nhb;
+    const int k = km / p.mpc, m0 = km - k * p.mpc;
+    const int cs = p.cu_chunk[k], ce = p.cu_chunk[k + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cs0 = p.cu_chunk[lo], ce0 = p.cu_chunk[lo + 1];
-    const int bs = cs0 + ((t0 - cs0) / 128) * 128;  // start of the block holding t0
-    for (int hb = warp; hb * 32 < p.H; hb += 4) {
-        const int h = hb * 32 + lane;
-        const bool hv = h < p.H;
-        const float Ah = hv ? p.A[h] : 0.f;
-        const float bias = (hv && p.dt_bias) ? p.dt_bias[h] : 0.f;
-        const __nv_bfloat16 *dth = p.dt + (hv ? h : 0);
-        int k = lo, ce = ce0;
-        int nbs = min(bs + 128, ce);  // the next block start after bs
-        float run = 0.f;
-        // Tokens [ta, ta + m), m <= 32: the dt loads are all issued first, then the running sum
-        // restarts at every block start (at a chunk's end the next chunk starts a block).
-        auto walk = [&](int ta, int m, bool out) {
-            float dv[32];
+    const int h = hb * 32 + lane;
+    const bool hv = h < p.H;
+    const float Ah = hv ? p.A[h] : 0.f;
+    const float bias = (hv && p.dt_bias) ? p.dt_bias[h] : 0.f;
+    const __nv_bfloat16 *dth = p.dt + (hv ? h : 0);
+    for (int tb = cs + 128 * m0; tb < ce; tb += 128 * p.mpc) {
+        const int L = min(128, ce - tb);
+        const int ta = tb + 32 * warp;
+        const int mw = max(0, min(32, tb + L - ta));  // this warp's tokens
+        float dv[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dv[j] = j < m ? __bfloat162float(dth[(size_t)(ta + j) * p.H]) : 0.f;
+        for (int j = 0; j < 32; ++j) dv[j] = j < mw ? __bfloat162float(dth[(size_t)(ta + j) * p.H]) : 0.f;
+        float run = 0.f;  // the cumsum within this warp's 32 tokens
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (j < m) {
-                    if (ta + j == nbs) {
-                        run = 0.f;
-                        if (nbs == ce && k + 1 < p.K) ce = p.cu_chunk[++k + 1];
-                        nbs = min(nbs + 128, ce);
-                    }
-                    const float d = fast_delta(dv[j] + bias, p.dt_softplus, p.dt_min, p.dt_max);
-                    run += d * Ah;
-                    if (out) {
-                        sC[warp][lane][j] = run;
-                        sD[warp][lane][j] = d;
-                    }
-                }
+        for (int j = 0; j < 32; ++j) {
+            if (j < mw) {
+                const float d = fast_delta(dv[j] + bias, p.dt_softplus, p.dt_min, p.dt_max);
+                run = fmaf(d, Ah, run);
+                sC[lane][32 * warp + j] = run;
+                sD[lane][32 * warp + j] = d;
             }
-        };
-        for (int ta = bs; ta < t0; ta += 32) walk(ta, min(32, t0 - ta), false);
-        for (int seg = 0; seg < n; seg += 32) {
-            const int m = min(32, n - seg);
-            walk(t0 + seg, m, true);
-            __syncwarp();
-            for (int hh = 0; hh < 32; ++hh) {
-                const int h2 = hb * 32 + hh;
-                if (h2 < p.H && lane < m) {
-                    const size_t o = (size_t)h2 * p.T + t0 + seg + lane;
-                    p.cum[o] = sC[warp][hh][lane];
-                    p.delta[o] = sD[warp][hh][lane];
-                }
-            }
-            __syncwarp();
         }
+        sTail[warp][lane] = run;
+        __syncthreads();
+        // coalesced stores: warp w writes heads w, w + 4, ...; a token adds the totals of the
+        // 32-token quarters before its own
+        for (int hh = warp; hh < 32; hh += 4) {
+            const int h2 = hb * 32 + hh;
+            if (h2 >= p.H) break;
+            float carry = 0.f;
+            for (int u0 = 0; u0 < L; u0 += 32) {
+                const int u = u0 + lane;
+                if (u < L) {
+                    const size_t o = (size_t)h2 * p.T + tb + u;
+                    p.cum[o] = sC[hh][u] + carry;
+                    p.delta[o] = sD[hh][u];
+                }
+                carry += sTail[u0 >> 5][hh];
+            }
+        }
+        __syncthreads();  // the staging arrays are reused by the next piece
     }
 }
 
@@ -767,10 +915,36 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
 
 static size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
 
+// Segments per sequence.  One CTA per (sequence, head) fills the GPU when there are at least
+// half as many of them as SMs; below that each sequence is cut into k segments of whole blocks
+// (k CTAs per (sequence, head), at most 8, and on average at least two blocks each), at the
+// price of the segment pass.  0 SMs (no device) means no split.
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int tc_prefill_segments(const ssd_prefill_args &a) {
+    const long long sh = (long long)a.num_seqs * a.nheads;
+    const int sms = sm_count();
+    if (sh <= 0 || 2 * sh > sms) return 1;
+    long long k = sms / sh;
+    const long long avg_blocks = (long long)a.total_tokens / a.num_seqs / kL;
+    k = std::min(k, std::max(1ll, avg_blocks / 2));
+    return (int)std::min(k, 8ll);
+}
+
 size_t tc_prefill_workspace(const ssd_prefill_args &a) {
     const size_t bc = (size_t)a.total_tokens * a.ngroups * kN * 2;
     const size_t ht = (size_t)a.total_tokens * a.nheads * 4;
-    return 2 * up256(bc) + 2 * up256(ht);
+    const int k = tc_prefill_segments(a);
+    const size_t sg = (size_t)a.num_seqs * (k - 1) * a.nheads;
+    return 2 * up256(bc) + 2 * up256(ht) + (k > 1 ? up256(sg * kP * kN * 4) + up256(sg * 4) : 0);
 }
 
 bool tc_prefill_supported(const ssd_prefill_args &a) {
@@ -805,8 +979,12 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
         q.cu_chunk = a.cu_chunk_seqlens;
         q.cum = cum;
         q.delta = delta;
-        const unsigned blocks = (unsigned)((a.total_tokens + 127) / 128);
-        prep_kernel<<<blocks, kPrepThreads, 0, s>>>(q);
+        q.mpc = std::max(1, std::min((a.chunk_size + kL - 1) / kL, 64));
+        q.nscan = a.num_chunks * q.mpc * ((a.nheads + 31) / 32);
+        const int sms = std::max(sm_count(), 1);
+        const size_t conv = std::min<size_t>(((size_t)a.total_tokens * q.row16 + 4 * kPrepThreads - 1) / (4 * kPrepThreads),
+                                             (size_t)sms * 8);
+        prep_kernel<<<(unsigned)(q.nscan + std::max<size_t>(conv, 1)), kPrepThreads, 0, s>>>(q);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -842,12 +1020,25 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
     p.wait_limit = a.wait_limit_cycles > 0 ? (long long)a.wait_limit_cycles : 2000000000ll;
     p.cum = cum;
     p.delta = delta;
-    auto kernel = p.z ? ssd_prefill_tc_kernel<true> : ssd_prefill_tc_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
+    p.nseg = tc_prefill_segments(a);
+    p.seg_state = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(delta) + up256(ht));
+    p.seg_decay = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(p.seg_state) +
+                                            up256((size_t)a.num_seqs * (p.nseg - 1) * a.nheads * kP * kN * 4));
     const long long grid = (long long)a.num_seqs * a.nheads;
     if (grid <= 0) return cudaSuccess;
-    kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(mX, mB, mC, p);
+    cudaError_t e;
+    if (p.nseg > 1) {
+        auto seg_kernel = ssd_prefill_tc_kernel<false, true>;
+        e = cudaFuncSetAttribute(seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        seg_kernel<<<(unsigned)(grid * (p.nseg - 1)), kThreads, kSmemBytes, s>>>(mX, mB, mC, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    auto kernel = p.z ? ssd_prefill_tc_kernel<true, false> : ssd_prefill_tc_kernel<false, false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kernel<<<(unsigned)(grid * p.nseg), kThreads, kSmemBytes, s>>>(mX, mB, mC, p);
     return cudaGetLastError();
 }
 
