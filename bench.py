@@ -81,18 +81,21 @@ def _sm_max_mhz():
 
 # ------------------------------------------------------------- byte counts --
 
-# DRAM traffic of one prefill call, from one ncu capture of the fused kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum = 3.471 GB for 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256), scaled
-# by tokens (x, y, B/C and one state per chunk all grow with them), plus the B/C pre-conversion, which
-# streams 2*T*G*N*2 bytes in and as many out.  Only for that head configuration and kernel version.
-FUSED_TRAFFIC_PER_TOKEN = 3.471e9 / 65536
+# DRAM traffic of one prefill call (tensor-core path, no segment split), from one ncu capture of both
+# its kernels on 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256: prep_kernel 285,269,760 B read +
+# 286,149,120 B written; ssd_prefill_tc_kernel 1,422,029,056 B read + 2,092,092,416 B written.  Scaled by
+# tokens (x, y, B/C, delta and one state per 256-token chunk all grow with them).  Only for that head
+# configuration and this kernel version; the summary is in profiles/.
+PREFILL_TRAFFIC_PER_TOKEN = (285269760 + 286149120 + 1422029056 + 2092092416) / 65536
+PREFILL_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of prep_kernel and ssd_prefill_tc_kernel "
+                          "on 8 x 8192 tokens, scaled by tokens")
 SM_MAX_MHZ = 2070.0  # GB300's maximum SM clock, where the measured-peaks file does not give it
 
 
 def prefill_traffic(T, H, P, N, G):
     if (H, P, N, G) != (128, 64, 128, 8):
         return None
-    return FUSED_TRAFFIC_PER_TOKEN * T + 4.0 * T * G * N * 2
+    return PREFILL_TRAFFIC_PER_TOKEN * T
 
 
 def prefill_bytes(T, K, H, P, N, G, elt, init_reads=0):
@@ -106,6 +109,13 @@ def prefill_bytes(T, K, H, P, N, G, elt, init_reads=0):
 # head, four dense products on full 128-row tiles: S = C B^T (128 x 128, K = N), Y1 = P X
 # (128 x P, K = 128), Y2 = C Hprev^T (128 x P, K = N) and dS = B^T (w x) (N x P, K = 128).
 TC_BLOCK = 128
+
+
+def prefill_method_flops(T, H, P, N, G, Q=TC_BLOCK):
+    """The method's own flops at internal block Q: per token G Q N (the causal half of C B^T per
+    group), H Q P (its causal product with delta x per head) and 4 H P N (the chunk-state update and
+    C . h_prev) -- no masked halves, no per-head recomputation of C B^T."""
+    return T * (G * Q * N + H * Q * P + 4 * H * P * N)
 
 
 def prefill_mma_flops(cu_chunk_seqlens, H, P, N):
@@ -739,6 +749,7 @@ def gpu_arm(args, rank, world, dist_on):
     hbm, peak_kind = _peaks()
     bf16, bf16_kind = _bf16_peak()
     pre_flops = prefill_mma_flops(st.meta["cu_chunk_seqlens"], H, P, N)
+    method_flops = prefill_method_flops(T, H, P, N, G)
     pre_mean = statistics.mean(pre_ms)
     dec_mean = statistics.mean(dec_ms) if R > 0 else 0.0
     achieved = pre_bytes / (pre_mean * 1e-3) / 1e9
@@ -757,13 +768,24 @@ def gpu_arm(args, rank, world, dist_on):
                                "unit": "TFLOP/s", "frac": pre_flops / (pre_mean * 1e-3) / 1e12 / bf16,
                                "flops": pre_flops, "peak_source": bf16_kind,
                                "what": "tcgen05 flops the fused kernel issues: four products per 128-token "
-                                       "block and head on full tiles, fp16 operands, fp32 accumulators"}},
+                                       "block and head on full tiles, fp16 operands, fp32 accumulators"},
+                    "method_flops": {"flops": method_flops,
+                                     "achieved": method_flops / (pre_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
+                                     "frac": method_flops / (pre_mean * 1e-3) / 1e12 / bf16,
+                                     "what": "G Q N + H Q P + 4 H P N per token at Q = 128: the causal halves "
+                                             "only, C B^T once per group"}},
+        "mixed_step": {"ms": ms_step, "prefill_alone_ms": pre_mean, "decode_alone_ms": dec_mean,
+                       "serial_ms": pre_mean + dec_mean,
+                       "bound_ms": pre_mean,
+                       "what": "the step with the decode beside the prefill; bound_ms is the step if the decode "
+                               "were hidden entirely (prefill alone), the most a single persistent launch could "
+                               "give"},
         "decode": {"state_updates_per_s": R / (dec_mean * 1e-3) if R else None, "ms": dec_mean,
                    "algorithmic_bytes": dec_bytes,
                    "hbm_frac": dec_bytes / (dec_mean * 1e-3) / 1e9 / hbm if R else None},
         "roofline": {"kernel": "ssd_prefill_varlen (%d kernels)" % st.prefill_kernels, "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": prefill_traffic(T, H, P, N, G),
+                     "traffic": prefill_traffic(T, H, P, N, G), "traffic_source": PREFILL_TRAFFIC_SOURCE,
                      "peak_source": peak_kind,
                      "units": "prefill algorithmic bytes per call / mean call time (CUDA events)"},
         "clocks": clk.summary(),

@@ -266,8 +266,10 @@ SSD_API ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *args, void *work
  * SSD_ERR_UNSUPPORTED for shapes the CUDA-core path does not take.
  *
  * The first call on each device looks up the array's device address (with
- * that device current) and keeps it; make that first call before any stream
- * capture.  All calls share the one array, and each call leaves its scratch
+ * that device current) and keeps it with the context it belongs to; make that
+ * first call before any stream capture.  After a device reset the next call
+ * finds a new context and looks the address up again (again before any
+ * capture).  All calls share the one array, and each call leaves its scratch
  * contents behind; nothing in it needs to start at zero, because with
  * metadata from ssd_chunk_metadata every value a call reads was written
  * earlier in the same call.  Calls whose kernels

@@ -9,16 +9,14 @@
 // with the W-1 inputs before the sequence's first token taken from its conv
 // state (zeros without one).
 //
-// HBM-bound streaming work, no contraction: each thread owns 8 consecutive
-// channels (one 16-byte vector) and a run of kRun consecutive tokens, keeping
-// the W-1 previous inputs in registers as a sliding window, so every input is
-// read once from HBM (plus W-1 rows of overlap per run) and every output written
-// once, coalesced across the warp.  The inputs of a batch of tokens are loaded
-// before any is used and the kernel is held to 4 CTAs per SM: together they
-// set how many bytes each SM keeps in flight, which is what bounds this kernel.  The outputs go straight to three tensors
-// (x, B, C), the layout the SSM calls take.  A second, small kernel then writes
-// the conv states at chunk ends and sequence ends: ordered after the first on
-// the stream, so all state reads precede all state writes.
+// HBM-bound streaming work, no contraction.  The varlen (prefill) form streams
+// TMA-loaded token tiles through shared memory (conv1d_tiled_kernel below); a
+// second, small kernel then writes the conv states at chunk ends and sequence
+// ends, ordered after the first on the stream, so all state reads precede all
+// state writes.  The decode form runs one thread per (request, 8 channels)
+// that reads its slot's history, applies the request's tokens and writes the
+// new window back (conv1d_decode_kernel).  The outputs go straight to three
+// tensors (x, B, C), the layout the SSM calls take.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
@@ -30,7 +28,6 @@ namespace {
 using namespace tc;
 
 constexpr int kVec = 8;        // channels per thread (16 bytes of bf16)
-constexpr int kRun = 64;       // tokens per thread (amortises the taps and the history reads)
 constexpr int kConvThreads = 128;
 
 struct ConvParams {
@@ -43,7 +40,6 @@ struct ConvParams {
 
 template <typename T> struct Vec8;
 template <> struct Vec8<__nv_bfloat16> {
-    static constexpr int kBatch = 8;  // tokens whose inputs are loaded before any is used
     struct Raw { uint4 u; };
     static __device__ __forceinline__ Raw load_raw(const __nv_bfloat16 *p) { return {*reinterpret_cast<const uint4 *>(p)}; }
     static __device__ __forceinline__ void unpack(const Raw &r, float (&v)[kVec]) {
@@ -81,7 +77,6 @@ template <> struct Vec8<__nv_bfloat16> {
     }
 };
 template <> struct Vec8<float> {
-    static constexpr int kBatch = 4;
     struct Raw { float4 a, b; };
     static __device__ __forceinline__ Raw load_raw(const float *p) {
         return {reinterpret_cast<const float4 *>(p)[0], reinterpret_cast<const float4 *>(p)[1]};
@@ -135,38 +130,21 @@ __device__ __forceinline__ int history_slot(const ConvParams &p, int r, bool rep
     return s;
 }
 
-// input j steps before token t of sequence r (start s0), for the 8 channels at c0: the
-// token itself when it is inside the sequence, else row (W-1) - (s0 - tau) of the history
+// ---- decode: one thread per (request, 8 channels) ------------------------------------------
+// A request's W-1 history rows come from its slot, its tokens follow, and the window after its
+// last token goes back to the same slot: the thread reads every row it writes before writing
+// it, so no second kernel is needed.  One CTA row of threads per request keeps every request
+// (and its slot's latency) in flight at once; padding requests (null slot) read and write nothing.
 template <typename Tin, int W>
-__device__ __forceinline__ void input_before(const Tin *xbc, const Tin *state, int hslot, int D, int s0, int tau,
-                                             int c0, float (&v)[kVec]) {
-    if (tau >= s0) {
-        Vec8<Tin>::load(xbc + (size_t)tau * D + c0, v);
-    } else if (hslot >= 0) {
-        Vec8<Tin>::load(state + ((size_t)hslot * (W - 1) + (W - 1) - (s0 - tau)) * D + c0, v);
-    } else {
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) v[i] = 0.f;
-    }
-}
-
-template <typename Tin, int W>
-__global__ void __launch_bounds__(kConvThreads, 4) conv1d_kernel(const Tin *__restrict__ xbc,
-                                                              const Tin *__restrict__ state, Tin *__restrict__ x_out,
-                                                              Tin *__restrict__ B_out, Tin *__restrict__ C_out,
-                                                              ConvParams p) {
+__global__ void __launch_bounds__(kConvThreads) conv1d_decode_kernel(const Tin *__restrict__ xbc, Tin *state,
+                                                                     Tin *__restrict__ x_out, Tin *__restrict__ B_out,
+                                                                     Tin *__restrict__ C_out, ConvParams p) {
     const int vec = blockIdx.x * kConvThreads + threadIdx.x;
-    const int t0 = blockIdx.y * kRun;
-    if (vec * kVec >= p.D || t0 >= p.T) return;
+    const int r = blockIdx.y;
+    if (vec * kVec >= p.D) return;
+    const int hslot = history_slot(p, r, vec == 0);
+    if (hslot < 0) return;  // padding (or an out-of-range slot, reported)
     const int c0 = vec * kVec;
-    float w[W][kVec], b[kVec];
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) {
-#pragma unroll
-        for (int k = 0; k < W; ++k) w[k][i] = p.weight[(size_t)(c0 + i) * W + k];
-        b[i] = p.bias ? p.bias[c0 + i] : 0.f;
-    }
-    // output tensor and column of these channels
     Tin *out;
     int ocol, ostride;
     if (c0 < p.dim_x) {
@@ -176,59 +154,41 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv1d_kernel(const Tin *__re
     } else {
         out = C_out, ocol = c0 - p.dim_x - p.dim_bc, ostride = p.dim_bc;
     }
-    const int t1 = min(t0 + kRun, p.T);
-    int r = p.decode ? t0 / p.tpr : seq_of(p.cu_seqlens, p.S, t0);
-    int s0 = seq_start(p, r), e0 = seq_end(p, r);
-    int hslot = history_slot(p, r, vec == 0);
+    Tin *slot = state + (size_t)hslot * (W - 1) * p.D + c0;
     float win[W - 1][kVec];  // win[0] oldest
 #pragma unroll
-    for (int j = 0; j < W - 1; ++j) input_before<Tin, W>(xbc, state, hslot, p.D, s0, t0 - (W - 1) + j, c0, win[j]);
-    constexpr int kB = Vec8<Tin>::kBatch;
-    for (int tb = t0; tb < t1; tb += kB) {
-        // the batch's inputs first: kB independent 16-byte loads in flight per thread
-        typename Vec8<Tin>::Raw raw[kB];
+    for (int j = 0; j < W - 1; ++j) Vec8<Tin>::load(slot + (size_t)j * p.D, win[j]);
+    float w[W][kVec], b[kVec];
 #pragma unroll
-        for (int j = 0; j < kB; ++j)
-            if (tb + j < t1) raw[j] = Vec8<Tin>::load_raw(xbc + (size_t)(tb + j) * p.D + c0);
+    for (int i = 0; i < kVec; ++i) {
 #pragma unroll
-        for (int j = 0; j < kB; ++j) {
-            const int t = tb + j;
-            if (t >= t1) break;
-            if (t >= e0) {  // next sequence (empty ones have no tokens to visit)
-                do {
-                    if (r + 1 >= p.S) {  // cu_seqlens does not end at T
-                        if (vec == 0) report(p.err, SSD_DEVERR_METADATA);
-                        return;
-                    }
-                    ++r;
-                    s0 = seq_start(p, r);
-                    e0 = seq_end(p, r);
-                } while (e0 <= t);
-                hslot = history_slot(p, r, vec == 0);
-#pragma unroll
-                for (int jj = 0; jj < W - 1; ++jj)
-                    input_before<Tin, W>(xbc, state, hslot, p.D, s0, t - (W - 1) + jj, c0, win[jj]);
-            }
-            float cur[kVec];
-            Vec8<Tin>::unpack(raw[j], cur);
-            float o[kVec];
-#pragma unroll
-            for (int i = 0; i < kVec; ++i) {
-                float acc = b[i];
-#pragma unroll
-                for (int k = 0; k < W - 1; ++k) acc = fmaf(w[k][i], win[k][i], acc);
-                acc = fmaf(w[W - 1][i], cur[i], acc);
-                o[i] = p.activation ? silu(acc) : acc;
-            }
-            if (hslot != -2) Vec8<Tin>::store(out + (size_t)t * ostride + ocol, o);
-#pragma unroll
-            for (int jj = 0; jj + 1 < W - 1; ++jj)
-#pragma unroll
-                for (int i = 0; i < kVec; ++i) win[jj][i] = win[jj + 1][i];
-#pragma unroll
-            for (int i = 0; i < kVec; ++i) win[W - 2][i] = cur[i];
-        }
+        for (int k = 0; k < W; ++k) w[k][i] = p.weight[(size_t)(c0 + i) * W + k];
+        b[i] = p.bias ? p.bias[c0 + i] : 0.f;
     }
+    for (int k = 0; k < p.tpr; ++k) {
+        const int t = r * p.tpr + k;
+        float cur[kVec], o[kVec];
+        Vec8<Tin>::load(xbc + (size_t)t * p.D + c0, cur);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) {
+            float acc = b[i];
+#pragma unroll
+            for (int kk = 0; kk < W - 1; ++kk) acc = fmaf(w[kk][i], win[kk][i], acc);
+            acc = fmaf(w[W - 1][i], cur[i], acc);
+            o[i] = p.activation ? silu(acc) : acc;
+        }
+        Vec8<Tin>::store(out + (size_t)t * ostride + ocol, o);
+#pragma unroll
+        for (int jj = 0; jj + 1 < W - 1; ++jj)
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) win[jj][i] = win[jj + 1][i];
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) win[W - 2][i] = cur[i];
+    }
+    // the window holds exact input values (widened from the token dtype), so storing them back
+    // reproduces the inputs bit for bit
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j) Vec8<Tin>::store(slot + (size_t)j * p.D, win[j]);
 }
 
 // ---- prefill: token tiles staged in shared memory ---------------------------------------
@@ -237,7 +197,8 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv1d_kernel(const Tin *__re
 // About two 256-thread CTAs per SM, each owning one channel tile and walking token tiles, keep
 // two tiles per CTA in flight ahead of the one being computed (about 137 KB of loads per SM),
 // which is what an HBM-bound stream needs on this part.  Each thread then computes 8 channels x (64 / groups) tokens from shared memory
-// with the same sliding window and sequence-boundary rules as conv1d_kernel.
+// with a sliding window of the W-1 previous inputs in registers, restarted from the history at
+// every sequence start.
 constexpr int kTileTok = 64;
 constexpr int kTileRowBytes = 512;
 constexpr int kTiledThreads = 256;
@@ -518,7 +479,6 @@ __global__ void __launch_bounds__(kConvThreads) conv_state_kernel(const Tin *__r
 template <typename Tin, int W>
 cudaError_t launch_w(const ssd_conv1d_args &a, const ConvParams &p, cudaStream_t st) {
     const int vecs = p.D / kVec;
-    const dim3 grid1((vecs + kConvThreads - 1) / kConvThreads, (p.T + kRun - 1) / kRun);
     const Tin *xbc = static_cast<const Tin *>(a.xbc);
     Tin *state = static_cast<Tin *>(a.conv_state);
     if (p.T > 0 && !p.decode) {
@@ -549,12 +509,12 @@ cudaError_t launch_w(const ssd_conv1d_args &a, const ConvParams &p, cudaStream_t
                                                                          static_cast<Tin *>(a.C_out), p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-    } else if (p.T > 0) {
-        conv1d_kernel<Tin, W><<<grid1, kConvThreads, 0, st>>>(xbc, state, static_cast<Tin *>(a.x_out),
-                                                              static_cast<Tin *>(a.B_out),
-                                                              static_cast<Tin *>(a.C_out), p);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+    } else if (p.T > 0) {  // decode: outputs and the new window in one kernel
+        const dim3 gridd((vecs + kConvThreads - 1) / kConvThreads, p.S);
+        conv1d_decode_kernel<Tin, W><<<gridd, kConvThreads, 0, st>>>(xbc, state, static_cast<Tin *>(a.x_out),
+                                                                     static_cast<Tin *>(a.B_out),
+                                                                     static_cast<Tin *>(a.C_out), p);
+        return cudaGetLastError();
     }
     const bool any_state = p.decode || p.out_slot || (p.chunk_slot && p.last_chunk);
     if (any_state && p.S > 0) {

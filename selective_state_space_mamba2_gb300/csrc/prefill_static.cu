@@ -7,6 +7,8 @@
 // no device allocator of its own.  The scratch lives in one file-scope
 // __device__ array of SSD_NOALLOC_SCRATCH_BYTES; every GPU that loads the
 // library holds it until the process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -17,22 +19,45 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BY
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device ordinal
+CUcontext g_scratch_ctx[kMaxDevices];  // context the address below was looked up in
+void *g_scratch_addr[kMaxDevices];     // device address of g_noalloc_scratch, per device ordinal
+
+// cuCtxGetCurrent, reached through the runtime (the library does not link the driver itself)
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    }
+    return fn;
+}
 
 // Device address of the scratch array on the current device.  The name of a
 // __device__ variable is only a host-side stand-in, so its address is asked
-// from the runtime once per device (with that device current) and kept.
+// from the runtime (with that device current) and kept, together with the
+// context it belongs to: after a device reset the device has a new primary
+// context with the module loaded anew, and the address is looked up again.
 cudaError_t scratch_on_current_device(void **addr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const CtxGetCurrentFn get_ctx = ctx_get_current();
+    if (!get_ctx) return cudaErrorDeviceUninitialized;
+    CUcontext ctx = nullptr;  // null until the runtime has made the device's context current
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!ctx || !g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // sets the primary context up if needed
         if (e != cudaSuccess) return e;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *addr = g_scratch_addr[dev];
     return cudaSuccess;

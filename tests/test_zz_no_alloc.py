@@ -2,9 +2,10 @@
 device memory at call time (an engine that reserved all free memory for its
 state cache, or a host with only the C ABI).  Its scratch is a fixed device
 array inside the library.  Called through the C ABI, it must agree with
-ssd_prefill_varlen (given caller workspace) on y and on every stored state,
-within the parity tolerance, on two calls in a row -- the second call finds
-the first call's leftovers in the shared array.  This file is collected last
+ssd_prefill_varlen (given caller workspace) and with the oracle on y and on
+every stored state, within the parity tolerance, on three calls in a row, each
+smaller than the one before -- every later call finds an earlier call's
+leftovers in the shared array.  This file is collected last
 so that a failure here cannot hide any other test's result."""
 import ctypes
 
@@ -55,15 +56,21 @@ def _compare_once(case):
     others = torch.ones(case["cache"].shape[0], dtype=torch.bool, device=DEV)
     others[w] = False
     assert torch.equal(case["cache"][others].view(torch.int32), start[others].view(torch.int32))
+    # and y and every stored state against the oracle directly
+    o_y, o_s, o_same, o_tol = PT.check_prefill(case, y, meta, start, case["cache"])
+    assert o_y <= o_tol and o_s <= o_tol and o_same, (o_y, o_s, o_same)
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+def test_noalloc_matches_workspace_entry_point_and_oracle_three_times():
     ssd.build()
-    # two different calls in a row (fp32, then bf16 with other sizes)
-    _compare_once(W.prefill_case(31, [150, 40, 300], [10, 0, 64], 4, 32, 64, 2, 64, dtype=torch.float32,
-                                 device=DEV, has_init=[True, False, True], num_slots=40))
+    # three different calls in a row, each smaller than the one before, so every scratch byte a
+    # later call reads was left there by an earlier one (which must not matter)
     _compare_once(W.prefill_case(32, [2048], [0], 48, 64, 128, 4, 2048, device=DEV, mode="default",
                                  has_init=[False], num_slots=4))
+    _compare_once(W.prefill_case(31, [150, 40, 300], [10, 0, 64], 4, 32, 64, 2, 64, dtype=torch.float32,
+                                 device=DEV, has_init=[True, False, True], num_slots=40))
+    _compare_once(W.prefill_case(34, [70, 33], [5, 0], 2, 16, 32, 1, 32, dtype=torch.float32, device=DEV,
+                                 has_init=[True, False], num_slots=12))
 
 
 def test_noalloc_refuses_calls_beyond_its_scratch():
