@@ -10,9 +10,11 @@
 // Memory behaviour: per live (request, head) the fp32 state [P, N] is read
 // once (float4, a warp covers 512 contiguous bytes) and written once per
 // token whose column slot is not null.  That traffic is the whole algorithmic
-// cost, so the kernel is HBM-bound; the arithmetic (one exp per token, one
-// FMA pair per state element, a warp-shuffle reduction over dstate for y)
-// hides under it.
+// cost, so the kernel is HBM-bound as long as the arithmetic per state element
+// (one FMA pair for the update, one for y) stays a few instructions: the
+// dstate = 128 instance has fixed indexing, reads B and C once per token and
+// reduces a warp's rows for y in one transposing shuffle pass; the general
+// instance serves the other dstate values.
 #include "common.cuh"
 
 namespace ssd {
@@ -154,10 +156,160 @@ __global__ void __launch_bounds__(kThreads, VPT >= 16 ? 2 : 4)
     }
 }
 
+// Sum of K per-row partials over the 32 lanes of a warp, transposing as it goes: each halving
+// step trades half of the lane's rows with the partner lane `o` away, so K values need log2(K)
+// shuffles for the first steps instead of K each.  On return, lane l holds in v[0] the full sum of
+// row (l >> (5 - log2 K)) & (K - 1).
+template <int K>
+__device__ __forceinline__ void warp_transpose_sum(float (&v)[K], int lane) {
+    int o = 16;
+#pragma unroll
+    for (int k = K; k > 1; k >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int q = 0; q < k / 2; ++q) {
+            const float send = up ? v[q] : v[q + k / 2];
+            const float keep = up ? v[q + k / 2] : v[q];
+            v[q] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+#pragma unroll
+    for (; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+}
+
+template <int K> struct Log2 { static constexpr int v = 1 + Log2<K / 2>::v; };
+template <> struct Log2<1> { static constexpr int v = 0; };
+
+// dstate = 128: a state row of one headdim index p is 128 floats, one float4 per lane of a warp,
+// so warp w owns the rows p = w + 8 i (i < RPW = headdim / 8) with fixed indexing.  B and C are
+// read once per token (lane l's four dstate entries), and the warp's RPW row sums for y come out of
+// one transposing reduction, each written by a single lane: no atomics, no zeroing of y.
+template <typename Tin, int RPW, bool kGate>
+__global__ void __launch_bounds__(kThreads, RPW >= 16 ? 2 : 4)
+    ssm_decode_n128_kernel(const ssm_decode_args a) {
+    const int r = blockIdx.x;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int P = 8 * RPW, N = 128;
+    const int H = a.nheads;
+    const int g = h / (H / a.ngroups);
+    const int tpr = a.tokens_per_req;
+
+    const int col = a.num_accepted_tokens ? a.num_accepted_tokens[r] : 0;
+    if (col < 0 || col >= a.state_indices_cols) {
+        if (tid == 0 && h == 0) report(a.err_word, SSD_DEVERR_COLUMN);
+        return;
+    }
+    const int32_t *row_slots = a.state_indices + (size_t)r * a.state_indices_cols;
+    const int32_t rs = row_slots[col];
+    if (rs == a.null_block_id) return;  // CUDA-graph padding row
+    if (rs < 0 || rs >= a.num_slots) {
+        if (tid == 0 && h == 0) report(a.err_word, SSD_DEVERR_SLOT);
+        return;
+    }
+
+    extern __shared__ __align__(16) float dsm[];
+    float *sx = dsm;                   // [kTokBatch][8][RPW]: x of row w + 8 i at [w][i]
+    float *sy = sx + kTokBatch * P;    // [kTokBatch][P]
+    float *sB = sy + kTokBatch * P;    // [kTokBatch][N]
+    float *sC = sB + kTokBatch * N;    // [kTokBatch][N]
+    float *sD = sC + kTokBatch * N;    // [kTokBatch] delta
+
+    constexpr int PN = P * N;
+    const size_t head_off = (size_t)h * PN;
+    float4 s[RPW];
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(a.state_cache + (size_t)rs * H * PN + head_off);
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) s[i] = src[(warp + 8 * i) * 32 + lane];
+    }
+    const float A = a.A[h];
+    const float Dh = a.D ? a.D[h] : 0.f;
+    const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
+    const Tin *x = static_cast<const Tin *>(a.x);
+    const Tin *dtp = static_cast<const Tin *>(a.dt);
+    const Tin *Bp = static_cast<const Tin *>(a.B);
+    const Tin *Cp = static_cast<const Tin *>(a.C);
+    const Tin *z = static_cast<const Tin *>(a.z);  // output gate or NULL
+    Tin *y = static_cast<Tin *>(a.y);
+    constexpr int kShift = 5 - Log2<RPW>::v;  // lanes below this bit share a reduced row
+    const int my_row = (lane >> kShift) & (RPW - 1);
+    const bool writer = (lane & ((1 << kShift) - 1)) == 0;
+
+    for (int k0 = 0; k0 < tpr; k0 += kTokBatch) {
+        const int kb = min(kTokBatch, tpr - k0);
+        if (k0 > 0) __syncthreads();  // the previous batch's readers of the staging arrays are done
+        for (int j = tid; j < kb * P; j += kThreads) {
+            const int kk = j / P, pp = j - kk * P;
+            const size_t row = (size_t)r * tpr + k0 + kk;
+            sx[kk * P + (pp & 7) * RPW + (pp >> 3)] = ldg_f32(x + (row * H + h) * P + pp);
+        }
+        for (int j = tid; j < kb * N; j += kThreads) {
+            const int kk = j / N, nn = j - kk * N;
+            const size_t row = (size_t)r * tpr + k0 + kk;
+            sB[kk * N + nn] = ldg_f32(Bp + (row * a.ngroups + g) * N + nn);
+            sC[kk * N + nn] = ldg_f32(Cp + (row * a.ngroups + g) * N + nn);
+        }
+        if (tid < kb) {
+            const size_t row = (size_t)r * tpr + k0 + tid;
+            sD[tid] = step_delta(ldg_f32(dtp + row * H + h) + bias, a.dt_softplus, a.dt_min, a.dt_max);
+        }
+        __syncthreads();
+        for (int kk = 0; kk < kb; ++kk) {
+            const float delta = sD[kk];
+            const float decay = __expf(delta * A);
+            const float4 b4 = reinterpret_cast<const float4 *>(sB + kk * N)[lane];
+            const float4 c4 = reinterpret_cast<const float4 *>(sC + kk * N)[lane];
+            const float *xw = sx + kk * P + warp * RPW;
+            float part[RPW];
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const float dx = delta * xw[i];
+                s[i].x = fmaf(decay, s[i].x, dx * b4.x);
+                s[i].y = fmaf(decay, s[i].y, dx * b4.y);
+                s[i].z = fmaf(decay, s[i].z, dx * b4.z);
+                s[i].w = fmaf(decay, s[i].w, dx * b4.w);
+                part[i] = s[i].x * c4.x + s[i].y * c4.y + s[i].z * c4.z + s[i].w * c4.w;
+            }
+            warp_transpose_sum<RPW>(part, lane);
+            if (writer) sy[kk * P + warp + 8 * my_row] = part[0];
+            const int32_t ws = row_slots[k0 + kk];
+            if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr)) {
+                float4 *dst = reinterpret_cast<float4 *>(a.state_cache + (size_t)ws * H * PN + head_off);
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) dst[(warp + 8 * i) * 32 + lane] = s[i];
+            }
+        }
+        __syncthreads();
+        for (int j = tid; j < kb * P; j += kThreads) {
+            const int kk = j / P, pp = j - kk * P;
+            const size_t o = (((size_t)r * tpr + k0 + kk) * H + h) * P + pp;
+            const float v = sy[j] + Dh * sx[kk * P + (pp & 7) * RPW + (pp >> 3)];
+            y[o] = from_f32<Tin>(kGate ? silu_gate(v, ldg_f32(z + o)) : v);
+        }
+    }
+}
+
+template <typename Tin, bool kGate>
+bool launch_n128(const ssm_decode_args &a, cudaStream_t st) {
+    dim3 grid(a.batch, a.nheads);
+    const size_t sm = decode_smem_bytes(a.headdim, a.dstate);
+    switch (a.headdim) {
+    case 8: ssm_decode_n128_kernel<Tin, 1, kGate><<<grid, kThreads, sm, st>>>(a); return true;
+    case 16: ssm_decode_n128_kernel<Tin, 2, kGate><<<grid, kThreads, sm, st>>>(a); return true;
+    case 32: ssm_decode_n128_kernel<Tin, 4, kGate><<<grid, kThreads, sm, st>>>(a); return true;
+    case 64: ssm_decode_n128_kernel<Tin, 8, kGate><<<grid, kThreads, sm, st>>>(a); return true;
+    case 128: ssm_decode_n128_kernel<Tin, 16, kGate><<<grid, kThreads, sm, st>>>(a); return true;
+    default: return false;
+    }
+}
+
 template <typename Tin>
 cudaError_t launch_typed(const ssm_decode_args &a, cudaStream_t st) {
     const int nvec = a.headdim * a.dstate / 4;
     const int vpt = (nvec + kThreads - 1) / kThreads;
+    if (a.dstate == 128 && (a.z ? launch_n128<Tin, true>(a, st) : launch_n128<Tin, false>(a, st)))
+        return cudaGetLastError();
     dim3 grid(a.batch, a.nheads);
     const size_t sm = decode_smem_bytes(a.headdim, a.dstate);
     if (a.z) {  // gated instances: y * silu(z)

@@ -53,7 +53,10 @@ def test_spec_decode_output_gate(dtype):
     assert nlive == 5 and e_y <= tol and e_s <= tol and same, (e_y, e_s, same)
 
 
-@pytest.mark.parametrize("N,P", [(16, 8), (64, 32), (256, 64)])
+# dstate 128 with headdim 8 .. 128 runs the fixed-index kernel (one instance per headdim); the
+# other sizes, headdim 48 among them, run the general one.
+@pytest.mark.parametrize("N,P", [(16, 8), (64, 32), (256, 64), (128, 8), (128, 16), (128, 32), (128, 48),
+                                 (128, 128)])
 def test_decode_other_state_sizes(N, P):
     case = W.decode_case(22, live=3, padded=4, tokens_per_req=2, H=2, P=P, N=N, G=1, num_slots=12,
                          device=DEV)
@@ -105,8 +108,24 @@ def test_spec_decode_batch_full_size_sampled():
     assert torch.equal(fp_after[mask], fp_before[mask])
 
 
-def test_bad_accepted_column_and_slot_are_reported():
-    case = W.decode_case(24, live=3, padded=3, tokens_per_req=2, H=2, P=16, N=16, G=1, num_slots=10,
+@pytest.mark.parametrize("N,P", [(16, 16), (128, 64)])
+def test_more_tokens_per_request_than_one_staging_batch(N, P):
+    """11 tokens per request: the kernels stage a request's tokens 8 at a time, so the state
+    carries over from one batch of staged tokens to the next."""
+    case = W.decode_case(25, live=3, padded=4, tokens_per_req=11, H=2, P=P, N=N, G=1, num_slots=40,
+                         device=DEV)
+    before = case["cache"].clone()
+    err = _err()
+    y = PT.run_decode(case, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    e_y, e_s, same, tol, nlive = PT.check_decode(case, y, before, case["cache"])
+    assert nlive == 3 and e_y <= tol and e_s <= tol and same, (e_y, e_s, same)
+
+
+@pytest.mark.parametrize("N,P", [(16, 16), (128, 64)])
+def test_bad_accepted_column_and_slot_are_reported(N, P):
+    case = W.decode_case(24, live=3, padded=3, tokens_per_req=2, H=2, P=P, N=N, G=1, num_slots=10,
                          device=DEV)
     case["num_accepted"][0] = 5
     case["state_indices"][1, 1] = 77
