@@ -354,7 +354,7 @@ typedef struct ssd_conv1d_args {
     int32_t null_block_id;
     /* device pointers */
     const void *xbc;       /* [T, D] with D = dim_x + 2 dim_bc, 16-byte aligned rows (D % 8 == 0) */
-    const float *weight;   /* [D, W] */
+    const float *weight;   /* [D, W], 16-byte aligned */
     const float *bias;     /* [D] or NULL */
     const int32_t *cu_seqlens;        /* [S+1] (ssd_conv1d_varlen) */
     const int32_t *cu_chunk_seqlens;  /* [K+1] or NULL (ssd_conv1d_varlen) */
@@ -428,7 +428,7 @@ typedef struct mamba1_args {
     const void *B;  /* [T, G, N], 16-byte aligned */
     const void *C;  /* [T, G, N], 16-byte aligned */
     const void *z;  /* [T, Dc] or NULL, 16-byte aligned: output gate */
-    const float *A; /* [Dc, N] */
+    const float *A; /* [Dc, N], 16-byte aligned */
     const float *D; /* [Dc] or NULL */
     const float *dt_bias;              /* [Dc] or NULL */
     const int32_t *cu_seqlens;         /* scan: [S+1] */

@@ -114,7 +114,7 @@ ssd_status_t check_conv(const ssd_conv1d_args *a, bool decode) {
     if (decode && (a->tokens_per_req < 1 || (int64_t)a->num_seqs * a->tokens_per_req != a->total_tokens))
         return SSD_ERR_INVALID_ARG;
     if (a->total_tokens == 0 && a->num_seqs == 0) return SSD_OK;
-    if (!a->xbc || !a->weight || !aligned16(a->xbc)) return SSD_ERR_INVALID_ARG;
+    if (!a->xbc || !a->weight || !aligned16(a->xbc) || !aligned16(a->weight)) return SSD_ERR_INVALID_ARG;
     if (a->total_tokens > 0 && (!a->x_out || !a->B_out || !a->C_out || !aligned16(a->x_out) ||
                                 !aligned16(a->B_out) || !aligned16(a->C_out)))
         return SSD_ERR_INVALID_ARG;
@@ -164,7 +164,7 @@ ssd_status_t check_mamba1(const mamba1_args *a, bool decode) {
     if (a->total_tokens == 0) return SSD_OK;
     if (!a->x || !a->dt || !a->B || !a->C || !a->A || !a->y) return SSD_ERR_INVALID_ARG;
     if (!aligned16(a->x) || !aligned16(a->dt) || !aligned16(a->B) || !aligned16(a->C) || !aligned16(a->y) ||
-        (a->z && !aligned16(a->z)))
+        !aligned16(a->A) || (a->z && !aligned16(a->z)))
         return SSD_ERR_INVALID_ARG;
     if (decode) {
         if (!a->state_indices || !a->state_cache || a->num_slots <= 0 || !aligned16(a->state_cache))

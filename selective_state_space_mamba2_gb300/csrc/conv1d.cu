@@ -158,11 +158,17 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_decode_kernel(const Tin *
     float win[W - 1][kVec];  // win[0] oldest
 #pragma unroll
     for (int j = 0; j < W - 1; ++j) Vec8<Tin>::load(slot + (size_t)j * p.D, win[j]);
-    float w[W][kVec], b[kVec];
+    // the thread's kVec x W weights are contiguous ([D, W] layout): W kVec / 4 16-byte loads
+    float wf[W * kVec], w[W][kVec], b[kVec];
+#pragma unroll
+    for (int j = 0; j < W * kVec / 4; ++j) {
+        const float4 v = reinterpret_cast<const float4 *>(p.weight + (size_t)c0 * W)[j];
+        wf[4 * j] = v.x; wf[4 * j + 1] = v.y; wf[4 * j + 2] = v.z; wf[4 * j + 3] = v.w;
+    }
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
 #pragma unroll
-        for (int k = 0; k < W; ++k) w[k][i] = p.weight[(size_t)(c0 + i) * W + k];
+        for (int k = 0; k < W; ++k) w[k][i] = wf[i * W + k];
         b[i] = p.bias ? p.bias[c0 + i] : 0.f;
     }
     for (int k = 0; k < p.tpr; ++k) {

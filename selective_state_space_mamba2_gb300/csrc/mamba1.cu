@@ -346,9 +346,9 @@ __global__ void __launch_bounds__(kCh) mamba1_update_kernel(const mamba1_args a)
     constexpr float kLog2e = 1.4426950408889634f;
     float2 h[N / 2], A2[N / 2];
     state_load2<N>(a.state_cache + ((size_t)rs * Dc + d) * N, h);
+    state_load2<N>(a.A + (size_t)d * N, A2);
 #pragma unroll
-    for (int i = 0; i < N / 2; ++i)
-        A2[i] = make_float2(a.A[(size_t)d * N + 2 * i] * kLog2e, a.A[(size_t)d * N + 2 * i + 1] * kLog2e);
+    for (int i = 0; i < N / 2; ++i) A2[i] = make_float2(A2[i].x * kLog2e, A2[i].y * kLog2e);
     const float Dd = a.D ? a.D[d] : 0.f;
     const float bias = a.dt_bias ? a.dt_bias[d] : 0.f;
     const Tin *x = static_cast<const Tin *>(a.x), *dt = static_cast<const Tin *>(a.dt);

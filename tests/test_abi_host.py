@@ -214,6 +214,7 @@ def _conv_args(**over):
     (dict(activation=2), B.SSD_ERR_INVALID_ARG),
     (dict(dtype=7), B.SSD_ERR_INVALID_ARG),
     (dict(xbc=0x10008), B.SSD_ERR_INVALID_ARG),
+    (dict(weight=0x10004), B.SSD_ERR_INVALID_ARG),  # weight rows are read in 16-byte pieces
     (dict(cu_seqlens=None), B.SSD_ERR_INVALID_ARG),
     (dict(conv_state=None), B.SSD_ERR_INVALID_ARG),  # slots without a state tensor
     (dict(chunk_slot=0x10000), B.SSD_ERR_INVALID_ARG),  # chunk slots without chunk metadata
@@ -277,6 +278,7 @@ def test_mamba1_scan_host_validation(lib, over, code):
     (dict(state_indices=None), B.SSD_ERR_INVALID_ARG),
     (dict(state_cache=None), B.SSD_ERR_INVALID_ARG),
     (dict(dstate=32), B.SSD_ERR_UNSUPPORTED),
+    (dict(A=0x10004), B.SSD_ERR_INVALID_ARG),  # A rows are read in 16-byte pieces
 ])
 def test_mamba1_update_host_validation(lib, over, code):
     a = _m1_args(**over)
