@@ -92,8 +92,8 @@ constexpr int kCbStages = 2, kXStages = 3;
 constexpr uint32_t OFF_X = kCbStages * CB_STAGE;
 constexpr uint32_t OFF_XW = OFF_X + kXStages * X_STAGE;  // w x (fp16)
 constexpr uint32_t OFF_H = OFF_XW + 16384;   // fp16 state entering the block
-constexpr uint32_t OFF_F = OFF_H + 16384;    // column factors, c_t and delta_t: [2 blocks][3][128]
-constexpr uint32_t OFF_E = OFF_F + 3072;     // exp(c_t) per block, ring of 4 [4][128]
+constexpr uint32_t OFF_F = OFF_H + 16384;    // column factors (two kinds), c_t and delta_t: [2 blocks][4][128]
+constexpr uint32_t OFF_E = OFF_F + 4096;     // exp(c_t) per block, ring of 4 [4][128]
 constexpr uint32_t OFF_DEC = OFF_E + 2048;   // exp(c_L) per block, ring of 4
 constexpr uint32_t OFF_TM = OFF_DEC + 16;    // TMEM base address
 constexpr uint32_t OFF_INFO = OFF_TM + 16;   // the CTA's part of its sequence [4]
@@ -496,10 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float c = rv.c, delta = rv.d, c_last = rv.g[3];
             if constexpr (!kState) {
-                float *sF = sFCD + (i & 1) * 384, *sCc = sF + 128, *sDl = sF + 256;
+                float *sF = sFCD + (i & 1) * 512, *sCc = sF + 128, *sDl = sF + 256, *sF2 = sF + 384;
                 sF[t] = __expf(rv.g[q] - c) * delta;  // column factor of column t (relative to its group's end)
                 sCc[t] = c;
                 sDl[t] = delta;
+                // column factor of column t relative to its group's first row (the diagonal group)
+                sF2[t] = __expf(__shfl_sync(0xffffffffu, c, 0) - c) * delta;
                 sE[(i % kRing) * 128 + t] = __expf(c);  // carried-state factor of row t (consumer)
             }
             if (t == 0) sDec[i % kRing] = __expf(c_last);
@@ -585,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[32], pk[16];
                 tmem_ld32(tm + lane_base + colS + 32 * j, v);
                 const float R = __expf(c - (j == 0 ? rv.g[0] : (j == 1 ? rv.g[1] : rv.g[2])));
-                const float4 *f4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 384 + 32 * j);
+                const float4 *f4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 512 + 32 * j);
                 tmem_ld_wait();
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -596,26 +598,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_st16(tm + lane_base + colS + 16 * j, pk);
             }
-            {  // the diagonal group j = q: one exponential per element, the mask by select
+            {  // the diagonal group j = q, the mask by select
                 uint32_t v[32], pk[16];
                 tmem_ld32(tm + lane_base + colS + 32 * q, v);
-                const float4 *c4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 384 + 128 + 32 * q);
-                const float4 *d4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 384 + 256 + 32 * q);
-                tmem_ld_wait();
+                // exp(c_t - c_s) = exp(c_t - c_b) exp(c_b - c_s), b the group's first row: both factors
+                // stay normal fp32 numbers while the group's total decay c_b - c_e is at most 80;
+                // beyond that, one exponential per element.  The same for the whole warp.
+                const float cb = __shfl_sync(0xffffffffu, c, 0);
+                if (cb - rv.g[q] <= 80.f) {
+                    const float R2 = __expf(c - cb);
+                    const float4 *f4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 512 + 384 + 32 * q);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {
-                    const float4 cs = c4[u4], ds = d4[u4];
-                    const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, dv[4] = {ds.x, ds.y, ds.z, ds.w};
-                    float pv[4];
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 f = f4[u4];
+                        const float fv[4] = {f.x, f.y, f.z, f.w};
+                        float pv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int u = 4 * u4 + e;
-                        const float ex = __expf(fminf(c - cv[e], 0.f));
-                        const float val = __uint_as_float(v[u]) * ex * dv[e];
-                        pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
+                        for (int e = 0; e < 4; ++e) {
+                            const int u = 4 * u4 + e;
+                            const float val = __uint_as_float(v[u]) * R2 * fv[e];  // at most |S| delta for u <= lane
+                            pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
+                        }
+                        pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
+                        pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
                     }
-                    pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
-                    pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
+                } else {
+                    const float4 *c4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 512 + 128 + 32 * q);
+                    const float4 *d4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 512 + 256 + 32 * q);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 cs = c4[u4], ds = d4[u4];
+                        const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, dv[4] = {ds.x, ds.y, ds.z, ds.w};
+                        float pv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int u = 4 * u4 + e;
+                            const float ex = __expf(fminf(c - cv[e], 0.f));
+                            const float val = __uint_as_float(v[u]) * ex * dv[e];
+                            pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
+                        }
+                        pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
+                        pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
+                    }
                 }
                 tmem_st16(tm + lane_base + colS + 16 * q, pk);
             }
