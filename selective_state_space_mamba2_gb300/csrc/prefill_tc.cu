@@ -592,9 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const float4 f = f4[u];
-                    pk[2 * u] = pack_f16_sat(__uint_as_float(v[4 * u]) * f.x * R, __uint_as_float(v[4 * u + 1]) * f.y * R);
-                    pk[2 * u + 1] =
-                        pack_f16_sat(__uint_as_float(v[4 * u + 2]) * f.z * R, __uint_as_float(v[4 * u + 3]) * f.w * R);
+                    const float2 a = mul_f2(mul_f2(make_float2(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1])),
+                                                   make_float2(f.x, f.y)), make_float2(R, R));
+                    const float2 b = mul_f2(mul_f2(make_float2(__uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])),
+                                                   make_float2(f.z, f.w)), make_float2(R, R));
+                    pk[2 * u] = pack_f16_sat(a.x, a.y);
+                    pk[2 * u + 1] = pack_f16_sat(b.x, b.y);
                 }
                 tmem_st16(tm + lane_base + colS + 16 * j, pk);
             }
@@ -612,12 +615,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u4 = 0; u4 < 8; ++u4) {
                         const float4 f = f4[u4];
-                        const float fv[4] = {f.x, f.y, f.z, f.w};
+                        // at most |S| delta for u <= lane
+                        const float2 a = mul_f2(mul_f2(make_float2(__uint_as_float(v[4 * u4]), __uint_as_float(v[4 * u4 + 1])),
+                                                       make_float2(R2, R2)), make_float2(f.x, f.y));
+                        const float2 b = mul_f2(mul_f2(make_float2(__uint_as_float(v[4 * u4 + 2]), __uint_as_float(v[4 * u4 + 3])),
+                                                       make_float2(R2, R2)), make_float2(f.z, f.w));
+                        const float vals[4] = {a.x, a.y, b.x, b.y};
                         float pv[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int u = 4 * u4 + e;
-                            const float val = __uint_as_float(v[u]) * R2 * fv[e];  // at most |S| delta for u <= lane
+                            const float val = vals[e];
                             pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
                         }
                         pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
@@ -706,7 +714,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld64(tm + lane_base + COL_DS, d);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 64; ++e) st[e] = fmaf(decay, st[e], __uint_as_float(d[e]));
+                for (int e = 0; e < 64; e += 2) {
+                    const float2 u = fma_f2(make_float2(decay, decay), make_float2(st[e], st[e + 1]),
+                                            make_float2(__uint_as_float(d[e]), __uint_as_float(d[e + 1])));
+                    st[e] = u.x;
+                    st[e + 1] = u.y;
+                }
                 dprod *= decay;
                 tc_fence_before();
                 __syncwarp();
@@ -746,7 +759,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld64(tm + lane_base + COL_DS, d);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 64; ++e) st[e] = fmaf(decay, st[e], __uint_as_float(d[e]));
+                for (int e = 0; e < 64; e += 2) {
+                    const float2 u = fma_f2(make_float2(decay, decay), make_float2(st[e], st[e + 1]),
+                                            make_float2(__uint_as_float(d[e]), __uint_as_float(d[e + 1])));
+                    st[e] = u.x;
+                    st[e + 1] = u.y;
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -786,8 +804,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 4; ++cc) {
                     float yv[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        yv[u] = fmaf(e_row, __uint_as_float(y2[8 * cc + u]), __uint_as_float(y1[8 * cc + u]));
+                    for (int u = 0; u < 8; u += 2) {
+                        const float2 o = fma_f2(make_float2(e_row, e_row),
+                                                make_float2(__uint_as_float(y2[8 * cc + u]), __uint_as_float(y2[8 * cc + u + 1])),
+                                                make_float2(__uint_as_float(y1[8 * cc + u]), __uint_as_float(y1[8 * cc + u + 1])));
+                        yv[u] = o.x;
+                        yv[u + 1] = o.y;
+                    }
                     if (kGate) {  // output gate y * silu(z); rows past the block end read a clamped
                                   // token (no lane-dependent branch between tcgen05 loads) and are
                                   // never stored

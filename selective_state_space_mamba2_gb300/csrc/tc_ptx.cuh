@@ -81,6 +81,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
     return true;
 }
 
+// ------------------------------------------------------- packed fp32 ----
+// Two fp32 lanes in one instruction (each rounded as the scalar operation would be).
+__device__ __forceinline__ uint64_t f2_bits(float2 v) { return *reinterpret_cast<uint64_t *>(&v); }
+__device__ __forceinline__ float2 f2_from(uint64_t v) { return *reinterpret_cast<float2 *>(&v); }
+__device__ __forceinline__ float2 mul_f2(float2 a, float2 b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_from(r);
+}
+__device__ __forceinline__ float2 fma_f2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+    return f2_from(r);
+}
+
 // ---------------------------------------------------------------- fences ----
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -200,6 +200,17 @@ def test_tensor_core_path_large_delta():
     _run_and_check(case, dt_bias=bias)
 
 
+def test_tensor_core_path_decay_beyond_the_factored_range():
+    """Per-token decays delta |A| of about 40, 6, 1 and 0.1 for the four heads (dt_bias 2): a
+    32-token group then decays by about 1300, 200, 34 and 3 in the log domain.  The first two heads
+    exceed the range where the P pass factors exp(c_t - c_s) into a row and a column factor (80),
+    so their diagonal groups take one exponential per element; the others take the factored form."""
+    case = W.prefill_case(20, [700, 190], [0, 0], 4, 64, 128, 2, 256, device=DEV, num_slots=40)
+    case["A"] = torch.tensor([-20.0, -3.0, -0.5, -0.05], device=DEV)
+    bias = torch.full((4,), 2.0, device=DEV)
+    _run_and_check(case, dt_bias=bias)
+
+
 def test_non_finite_tokens_of_the_next_sequence_stay_out():
     """The last block of sequence 0 is short (200 = 128 + 72 tokens), so the
     128-row tiles of that block also hold sequence 1's first 56 tokens.  Those
