@@ -521,12 +521,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool live = t < L;
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
-                uint4 xh = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(sXs + sw128_offset(t, cc)));
-                uint4 xw = make_uint4(hmul2_u32(xh.x, w2), hmul2_u32(xh.y, w2), hmul2_u32(xh.z, w2),
-                                      hmul2_u32(xh.w, w2));
-                if (!live) xh = xw = make_uint4(0u, 0u, 0u, 0u);
+                const uint4 xh = bf16x8_to_f16x8(*reinterpret_cast<const uint4 *>(sXs + sw128_offset(t, cc)));
+                const uint4 xw = make_uint4(hmul2_u32(xh.x, w2), hmul2_u32(xh.y, w2), hmul2_u32(xh.z, w2),
+                                            hmul2_u32(xh.w, w2));
                 *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = xw;
                 if (!kState) *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = xh;
+            }
+            if (!live) {  // only in a sequence's last, short block: these rows become zeros
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    *reinterpret_cast<uint4 *>(sXW + sw128_offset(t, cc)) = make_uint4(0u, 0u, 0u, 0u);
+                    if (!kState) *reinterpret_cast<uint4 *>(sXs + sw128_offset(t, cc)) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             if constexpr (kState) {
                 // the segment pass: B's rows past a short block's end are cleared for M4 (no M1 reads
