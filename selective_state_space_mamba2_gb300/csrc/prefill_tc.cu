@@ -207,7 +207,8 @@ __device__ __forceinline__ void store_state_row(uint8_t *sH, int n, const float 
 template <bool kGate, bool kState>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY,
+                          const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nsg = kState ? p.nseg - 1 : p.nseg;  // segments with a CTA in this launch
@@ -836,23 +837,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
+            fence_proxy_async_smem();  // the staged rows are visible to the tensor-copy engine
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[Y1_FREE]);  // M2 of the next block may overwrite Y1
             named_bar_sync(BAR_CG, 128);  // y tile staged
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                const int row = rr * 16 + (t >> 3), cc = t & 7;
-                if (row < L) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(sY + sw128_offset(row, cc));
-                    *reinterpret_cast<uint4 *>(p.y + ((size_t)(tb + row) * p.H + h) * kP + 8 * cc) = v;
+            if (L == kL) {
+                // a whole block: one tensor copy of the tile; its issuer waits until the copy has
+                // read the slot before the slot is given back to the x ring
+                if (t == 0) {
+                    tma_store_3d(&tmY, sY, 0, h, tb);
+                    bulk_commit();
+                    bulk_wait_read();
                 }
+                __syncwarp();
+            } else {
+                // a short block: rows past its end belong to the next sequence and are not written
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int row = rr * 16 + (t >> 3), cc = t & 7;
+                    if (row < L) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(sY + sw128_offset(row, cc));
+                        *reinterpret_cast<uint4 *>(p.y + ((size_t)(tb + row) * p.H + h) * kP + 8 * cc) = v;
+                    }
+                }
+                fence_proxy_async_smem();  // this warp's reads of the slot come before the next TMA write
+                __syncwarp();
             }
-            fence_proxy_async_smem();  // this warp's reads of the slot come before the next TMA write
-            __syncwarp();
             if (lane == 0) mbar_arrive(&bar[EMPTY_X0 + i % kXStages]);
         }
         }
     }
+    if (warp == 4 && lane == 0) bulk_wait();  // the y tile copies this thread issued are complete
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -1007,7 +1022,7 @@ bool tc_prefill_supported(const ssd_prefill_args &a) {
 }
 
 cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s) {
-    CUtensorMap mX, mB, mC;
+    CUtensorMap mX, mB, mC, mY;
     const uint64_t T = (uint64_t)a.total_tokens;
     const size_t bc = (size_t)a.total_tokens * a.ngroups * kN * 2;
     const size_t ht = (size_t)a.total_tokens * a.nheads * 4;
@@ -1045,7 +1060,8 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
     }
     if (!make_tmap_bf16_3d(&mX, a.x, kP, a.nheads, T, (uint64_t)kP * 2, (uint64_t)a.nheads * kP * 2, 64, 1, kL) ||
         !make_tmap_f16_3d(&mB, Bh, kN, a.ngroups, T, (uint64_t)kN * 2, (uint64_t)a.ngroups * kN * 2, 64, 1, kL) ||
-        !make_tmap_f16_3d(&mC, Ch, kN, a.ngroups, T, (uint64_t)kN * 2, (uint64_t)a.ngroups * kN * 2, 64, 1, kL))
+        !make_tmap_f16_3d(&mC, Ch, kN, a.ngroups, T, (uint64_t)kN * 2, (uint64_t)a.ngroups * kN * 2, 64, 1, kL) ||
+        !make_tmap_bf16_3d(&mY, a.y, kP, a.nheads, T, (uint64_t)kP * 2, (uint64_t)a.nheads * kP * 2, 64, 1, kL))
         return cudaErrorInvalidValue;
     TcParams p;
     p.T = a.total_tokens;
@@ -1086,14 +1102,14 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
         auto seg_kernel = ssd_prefill_tc_kernel<false, true>;
         e = cudaFuncSetAttribute(seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        seg_kernel<<<(unsigned)(grid * (p.nseg - 1)), kThreads, kSmemBytes, s>>>(mX, mB, mC, p);
+        seg_kernel<<<(unsigned)(grid * (p.nseg - 1)), kThreads, kSmemBytes, s>>>(mX, mB, mC, mY, p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     auto kernel = p.z ? ssd_prefill_tc_kernel<true, false> : ssd_prefill_tc_kernel<false, false>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kernel<<<(unsigned)(grid * p.nseg), kThreads, kSmemBytes, s>>>(mX, mB, mC, p);
+    kernel<<<(unsigned)(grid * p.nseg), kThreads, kSmemBytes, s>>>(mX, mB, mC, mY, p);
     return cudaGetLastError();
 }
 
