@@ -183,6 +183,35 @@ struct RowVals {
     }
 };
 
+// The diagonal group of the P pass when the group's decay is beyond the factored range: one
+// exponential per element.  Out of line: it is rarely taken, and the P pass's common path stays
+// small in the instruction cache.  Reads S from s_col, writes P (fp16) to p_col; cc and dd are the
+// group's cumsum and delta values.  Called by a whole warp.
+__device__ __noinline__ void diag_group_per_element(uint32_t s_col, uint32_t p_col, const float *cc, const float *dd,
+                                                     float c, float Dh, int lane) {
+    uint32_t v[32], pk[16];
+    tmem_ld32(s_col, v);
+    const float4 *c4 = reinterpret_cast<const float4 *>(cc);
+    const float4 *d4 = reinterpret_cast<const float4 *>(dd);
+    tmem_ld_wait();
+#pragma unroll
+    for (int u4 = 0; u4 < 8; ++u4) {
+        const float4 cs = c4[u4], ds = d4[u4];
+        const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, dv[4] = {ds.x, ds.y, ds.z, ds.w};
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int u = 4 * u4 + e;
+            const float ex = __expf(fminf(c - cv[e], 0.f));
+            const float val = __uint_as_float(v[u]) * ex * dv[e];
+            pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
+        }
+        pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
+        pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
+    }
+    tmem_st16(p_col, pk);
+}
+
 // fp16 copy of a state row (dstate row n: its 64 headdim values) into the M3 operand tile
 __device__ __forceinline__ void store_state_row(uint8_t *sH, int n, const float (&st)[kP]) {
 #pragma unroll
@@ -609,13 +638,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st16(tm + lane_base + colS + 16 * j, pk);
             }
             {  // the diagonal group j = q, the mask by select
-                uint32_t v[32], pk[16];
-                tmem_ld32(tm + lane_base + colS + 32 * q, v);
                 // exp(c_t - c_s) = exp(c_t - c_b) exp(c_b - c_s), b the group's first row: both factors
                 // stay normal fp32 numbers while the group's total decay c_b - c_e is at most 80;
                 // beyond that, one exponential per element.  The same for the whole warp.
                 const float cb = __shfl_sync(0xffffffffu, c, 0);
                 if (cb - rv.g[q] <= 80.f) {
+                    uint32_t v[32], pk[16];
+                    tmem_ld32(tm + lane_base + colS + 32 * q, v);
                     const float R2 = __expf(c - cb);
                     const float4 *f4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 512 + 384 + 32 * q);
                     tmem_ld_wait();
@@ -638,27 +667,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
                         pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
                     }
+                    tmem_st16(tm + lane_base + colS + 16 * q, pk);
                 } else {
-                    const float4 *c4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 512 + 128 + 32 * q);
-                    const float4 *d4 = reinterpret_cast<const float4 *>(sFCD + (i & 1) * 512 + 256 + 32 * q);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
-                        const float4 cs = c4[u4], ds = d4[u4];
-                        const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, dv[4] = {ds.x, ds.y, ds.z, ds.w};
-                        float pv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int u = 4 * u4 + e;
-                            const float ex = __expf(fminf(c - cv[e], 0.f));
-                            const float val = __uint_as_float(v[u]) * ex * dv[e];
-                            pv[e] = (u < lane) ? val : ((u == lane) ? val + Dh : 0.f);
-                        }
-                        pk[2 * u4] = pack_f16_sat(pv[0], pv[1]);
-                        pk[2 * u4 + 1] = pack_f16_sat(pv[2], pv[3]);
-                    }
+                    diag_group_per_element(tm + lane_base + colS + 32 * q, tm + lane_base + colS + 16 * q,
+                                           sFCD + (i & 1) * 512 + 128 + 32 * q, sFCD + (i & 1) * 512 + 256 + 32 * q,
+                                           c, Dh, lane);
                 }
-                tmem_st16(tm + lane_base + colS + 16 * q, pk);
             }
             {
                 uint32_t zero[16];
