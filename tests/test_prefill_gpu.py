@@ -266,16 +266,21 @@ def test_bounded_waits_give_up_and_the_context_survives():
     _run_and_check(case)
 
 
-def test_sequences_split_across_ctas():
+@pytest.mark.parametrize("gate", [False, True])
+def test_sequences_split_across_ctas(gate):
     """Two sequences and eight heads are too few (sequence, head) pairs to fill the GPU, so each
     sequence is cut into segments of whole blocks that separate CTAs run: the long sequence's
     segments start mid-chunk from the state the segment pass carries in; the short one (one
     block) leaves most of its segments empty.  Initial states, unaligned computed prefixes,
-    "all" mode; y and every stored state against the oracle."""
+    "all" mode, with and without the output gate; y and every stored state against the oracle."""
     case = W.prefill_case(22, [2000, 100], [37, 300], 8, 64, 128, 2, 256, device=DEV,
                           has_init=[True, True], num_slots=64)
     t = {k: torch.from_numpy(v).to(DEV) for k, v in PT.prefill_metadata(case).items()}
     a = ssd.prefill_args(case["x"], case["dt"], case["A"], case["B"], case["C"], case["cu_seqlens"].to(DEV),
                          t["cu_chunk_seqlens"], t["seq_idx"], t["last_chunk_indices"], torch.empty_like(case["x"]))
     assert ssd.ssd_prefill_kernel_count(a) == 3  # the segment pass runs
-    _run_and_check(case)
+    if gate:
+        g = torch.Generator(device=DEV).manual_seed(7)
+        _run_and_check(case, z=(3.0 * torch.randn(case["x"].shape, generator=g, device=DEV)).to(case["x"].dtype))
+    else:
+        _run_and_check(case)
