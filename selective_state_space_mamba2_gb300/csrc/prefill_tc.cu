@@ -21,18 +21,21 @@
 //   M4  dS = B^T (w x),  w_s = exp(c_L - c_s) delta_s   [dstate x 64]   (SS, MN/MN)
 // and then y_t = Y1 + exp(c_t) Y2,   state <- exp(c_L) state + dS.
 //
-// Decays are always exponentials of non-positive differences.  For a
-// 32-column group j lying entirely at or below row t, exp(c_t - c_s) is split
-// at the group's last row e: exp(c_t - c_e) exp(c_e - c_s), both factors <= 1,
-// so only the diagonal group needs one exponential per element.
+// Decays are factored so that an element of P costs two multiplies.  For a
+// 32-column group j lying entirely below row t's group, exp(c_t - c_s) is split
+// at the group's last row e: exp(c_t - c_e) exp(c_e - c_s), both factors <= 1.
+// The diagonal group is split at its first row b instead (exp(c_t - c_b) <= 1,
+// exp(c_b - c_s) >= 1), which keeps both factors normal fp32 numbers while the
+// group's decay c_b - c_e is at most 80; beyond that it takes one exponential
+// per element, in an out-of-line function.
 //
 // Only the state itself is a serial dependency from block to block (64 FMAs
 // per thread); everything else is pipelined.  One CTA per SM, 320 threads:
 //   warps 0-3  "producer" warpgroup, one block ahead: the column factors from
 //              delta and c, w x and x -> fp16, the P pass (S -> P in TMEM, in place)
 //   warps 4-7  "consumer" warpgroup: state update, the fp16 state tile for
-//              the next block's M3, the chunk-boundary stores, y and its
-//              coalesced copy-out
+//              the next block's M3, the chunk-boundary stores, y (staged in the
+//              spent x slot and written by one tensor copy per whole block)
 //   warp 8     TMA producer: C/B tiles in two stages, x tiles in three (128-byte
 //              swizzle)
 //   warp 9     TMEM allocation (512 columns) and MMA issue
