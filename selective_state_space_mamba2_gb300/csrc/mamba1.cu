@@ -324,28 +324,48 @@ __global__ void __launch_bounds__(kCh) mamba1_scan_kernel(const mamba1_args a) {
     }
 }
 
+// Decode: one CTA per (kReq requests, 64 channels), one channel per thread.  A thread loads the
+// states of its requests (and A once) before computing any of them, so kReq state loads are in
+// flight per thread and the grid has kReq times fewer waves.
+constexpr int kReq = 2;
+
 template <typename Tin, int N, bool kGate>
 __global__ void __launch_bounds__(kCh) mamba1_update_kernel(const mamba1_args a) {
-    const int r = blockIdx.x, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     const int Dc = a.dim, G = a.ngroups;
     const int d = blockIdx.y * kCh + tid;
     const int g = d / (Dc / G);
     const int tpr = a.tokens_per_req;
-    const int col = a.num_accepted_tokens ? a.num_accepted_tokens[r] : 0;
-    if (col < 0 || col >= a.state_indices_cols) {
-        if (tid == 0 && blockIdx.y == 0) report(a.err_word, SSD_DEVERR_COLUMN);
-        return;
+    int32_t rs[kReq];
+    bool live[kReq];
+    bool any = false;
+#pragma unroll
+    for (int q = 0; q < kReq; ++q) {
+        const int r = blockIdx.x * kReq + q;
+        live[q] = false;
+        rs[q] = 0;
+        if (r >= a.num_seqs) continue;
+        const int col = a.num_accepted_tokens ? a.num_accepted_tokens[r] : 0;
+        if (col < 0 || col >= a.state_indices_cols) {
+            if (tid == 0 && blockIdx.y == 0) report(a.err_word, SSD_DEVERR_COLUMN);
+            continue;
+        }
+        const int32_t s0 = a.state_indices[(size_t)r * a.state_indices_cols + col];
+        if (s0 == a.null_block_id) continue;  // CUDA-graph padding row
+        if (s0 < 0 || s0 >= a.num_slots) {
+            if (tid == 0 && blockIdx.y == 0) report(a.err_word, SSD_DEVERR_SLOT);
+            continue;
+        }
+        live[q] = true;
+        rs[q] = s0;
+        any = true;
     }
-    const int32_t *row_slots = a.state_indices + (size_t)r * a.state_indices_cols;
-    const int32_t rs = row_slots[col];
-    if (rs == a.null_block_id) return;  // CUDA-graph padding row
-    if (rs < 0 || rs >= a.num_slots) {
-        if (tid == 0 && blockIdx.y == 0) report(a.err_word, SSD_DEVERR_SLOT);
-        return;
-    }
+    if (!any) return;
     constexpr float kLog2e = 1.4426950408889634f;
-    float2 h[N / 2], A2[N / 2];
-    state_load2<N>(a.state_cache + ((size_t)rs * Dc + d) * N, h);
+    float2 h[kReq][N / 2], A2[N / 2];
+#pragma unroll
+    for (int q = 0; q < kReq; ++q)
+        if (live[q]) state_load2<N>(a.state_cache + ((size_t)rs[q] * Dc + d) * N, h[q]);
     state_load2<N>(a.A + (size_t)d * N, A2);
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) A2[i] = make_float2(A2[i].x * kLog2e, A2[i].y * kLog2e);
@@ -355,19 +375,25 @@ __global__ void __launch_bounds__(kCh) mamba1_update_kernel(const mamba1_args a)
     const Tin *Bp = static_cast<const Tin *>(a.B), *Cp = static_cast<const Tin *>(a.C);
     const Tin *z = static_cast<const Tin *>(a.z);
     Tin *y = static_cast<Tin *>(a.y);
-    for (int k = 0; k < tpr; ++k) {
-        const size_t row = (size_t)r * tpr + k;
-        float Bt[N], Ct[N];
-        row_to_f32_ldg<N>(Bp + (row * G + g) * N, Bt);
-        row_to_f32_ldg<N>(Cp + (row * G + g) * N, Ct);
-        const float xv = ldg_f32(x + row * Dc + d);
-        const float delta = m1_delta<Tin>(ldg_f32(dt + row * Dc + d) + bias, a);
-        float yv = m1_step<N>(h, A2, delta, xv, Bt, Ct, Dd);
-        if (kGate) yv = silu_gate(yv, ldg_f32(z + row * Dc + d));
-        y[row * Dc + d] = from_f32<Tin>(yv);
-        const int32_t ws = row_slots[k];
-        if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr))
-            state_store2<N>(a.state_cache + ((size_t)ws * Dc + d) * N, h);
+#pragma unroll
+    for (int q = 0; q < kReq; ++q) {
+        if (!live[q]) continue;
+        const int r = blockIdx.x * kReq + q;
+        const int32_t *row_slots = a.state_indices + (size_t)r * a.state_indices_cols;
+        for (int k = 0; k < tpr; ++k) {
+            const size_t row = (size_t)r * tpr + k;
+            float Bt[N], Ct[N];
+            row_to_f32_ldg<N>(Bp + (row * G + g) * N, Bt);
+            row_to_f32_ldg<N>(Cp + (row * G + g) * N, Ct);
+            const float xv = ldg_f32(x + row * Dc + d);
+            const float delta = m1_delta<Tin>(ldg_f32(dt + row * Dc + d) + bias, a);
+            float yv = m1_step<N>(h[q], A2, delta, xv, Bt, Ct, Dd);
+            if (kGate) yv = silu_gate(yv, ldg_f32(z + row * Dc + d));
+            y[row * Dc + d] = from_f32<Tin>(yv);
+            const int32_t ws = row_slots[k];
+            if (slot_usable(ws, a.null_block_id, a.num_slots, tid == 0 ? a.err_word : nullptr))
+                state_store2<N>(a.state_cache + ((size_t)ws * Dc + d) * N, h[q]);
+        }
     }
 }
 
@@ -375,8 +401,9 @@ template <typename Tin, int N>
 cudaError_t launch_n(const mamba1_args &a, bool decode, cudaStream_t st) {
     const dim3 grid(a.num_seqs, a.dim / kCh);
     if (decode) {
-        if (a.z) mamba1_update_kernel<Tin, N, true><<<grid, kCh, 0, st>>>(a);
-        else mamba1_update_kernel<Tin, N, false><<<grid, kCh, 0, st>>>(a);
+        const dim3 dgrid((a.num_seqs + kReq - 1) / kReq, a.dim / kCh);
+        if (a.z) mamba1_update_kernel<Tin, N, true><<<dgrid, kCh, 0, st>>>(a);
+        else mamba1_update_kernel<Tin, N, false><<<dgrid, kCh, 0, st>>>(a);
     } else {
         if (a.z) mamba1_scan_kernel<Tin, N, true><<<grid, kCh, 0, st>>>(a);
         else mamba1_scan_kernel<Tin, N, false><<<grid, kCh, 0, st>>>(a);
