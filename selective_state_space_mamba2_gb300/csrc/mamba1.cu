@@ -21,9 +21,9 @@
 // 3 x 2 bytes of HBM traffic (x, dt, y in bf16), so the multi-function unit,
 // not HBM, sets the time at N = 16.
 //
-// Decode: one CTA per (request, 64 channels), the request's state read from
-// the slot its num_accepted_tokens column names, each token's state stored to
-// its own column: the routing of ssm_decode_update.
+// Decode: one CTA per (two requests, 64 channels), each request's state read
+// from the slot its num_accepted_tokens column names, each token's state
+// stored to its own column: the routing of ssm_decode_update.
 #include "common.cuh"
 
 namespace ssd {
