@@ -284,3 +284,16 @@ def test_sequences_split_across_ctas(gate):
         _run_and_check(case, z=(3.0 * torch.randn(case["x"].shape, generator=g, device=DEV)).to(case["x"].dtype))
     else:
         _run_and_check(case)
+
+
+def test_one_sequence_split_into_eight_segments():
+    """One 8192-token sequence and four heads: the split reaches its maximum of eight segments
+    (SMs / heads and tokens / 256 both allow more), so segment 7 starts from segment 0's end state
+    carried through six segment decays.  An initial state, "all" mode, chunk 256; y and all 32
+    chunk states against the oracle."""
+    case = W.prefill_case(23, [8192], [512], 4, 64, 128, 2, 256, device=DEV, has_init=[True], num_slots=48)
+    t = {k: torch.from_numpy(v).to(DEV) for k, v in PT.prefill_metadata(case).items()}
+    a = ssd.prefill_args(case["x"], case["dt"], case["A"], case["B"], case["C"], case["cu_seqlens"].to(DEV),
+                         t["cu_chunk_seqlens"], t["seq_idx"], t["last_chunk_indices"], torch.empty_like(case["x"]))
+    assert ssd.ssd_prefill_kernel_count(a) == 3
+    _run_and_check(case)
