@@ -924,11 +924,66 @@ constexpr int kPrepThreads = 128;  // 4 warps
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
     __shared__ float sC[32][129], sD[32][129];  // one block's outputs: 32 heads x 128 tokens (padded)
     __shared__ float sTail[4][32];              // per warp and head: the sum over its 32 tokens
-    if ((int)blockIdx.x >= p.nscan) {
-        // B and C -> fp16, grid-stride over 16-byte units, four of each in flight per thread
+    // The scan CTAs (the first nscan) compute their piece first.  When there are enough of them
+    // (large calls), every CTA then converts its grid-stride share of B and C, so the conversion's
+    // bandwidth-bound work runs beside the scan's latency-bound CTAs throughout the grid; small
+    // calls get conversion CTAs of their own after the scan CTAs.
+    if ((int)blockIdx.x < p.nscan) {
+        const int nhb = (p.H + 31) / 32;
+        const int hb = blockIdx.x % nhb;
+        const int km = blockIdx.x / nhb;
+        const int k = km / p.mpc, m0 = km - k * p.mpc;
+        const int cs = p.cu_chunk[k], ce = p.cu_chunk[k + 1];
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int h = hb * 32 + lane;
+        const bool hv = h < p.H;
+        const float Ah = hv ? p.A[h] : 0.f;
+        const float bias = (hv && p.dt_bias) ? p.dt_bias[h] : 0.f;
+        const __nv_bfloat16 *dth = p.dt + (hv ? h : 0);
+        for (int tb = cs + 128 * m0; tb < ce; tb += 128 * p.mpc) {
+            const int L = min(128, ce - tb);
+            const int ta = tb + 32 * warp;
+            const int mw = max(0, min(32, tb + L - ta));  // this warp's tokens
+            float dv[32];
+    #pragma unroll
+            for (int j = 0; j < 32; ++j) dv[j] = j < mw ? __bfloat162float(dth[(size_t)(ta + j) * p.H]) : 0.f;
+            float run = 0.f;  // the cumsum within this warp's 32 tokens
+    #pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j < mw) {
+                    const float d = fast_delta(dv[j] + bias, p.dt_softplus, p.dt_min, p.dt_max);
+                    run = fmaf(d, Ah, run);
+                    sC[lane][32 * warp + j] = run;
+                    sD[lane][32 * warp + j] = d;
+                }
+            }
+            sTail[warp][lane] = run;
+            __syncthreads();
+            // coalesced stores: warp w writes heads w, w + 4, ...; a token adds the totals of the
+            // 32-token quarters before its own
+            for (int hh = warp; hh < 32; hh += 4) {
+                const int h2 = hb * 32 + hh;
+                if (h2 >= p.H) break;
+                float carry = 0.f;
+                for (int u0 = 0; u0 < L; u0 += 32) {
+                    const int u = u0 + lane;
+                    if (u < L) {
+                        const size_t o = (size_t)h2 * p.T + tb + u;
+                        p.cum[o] = sC[hh][u] + carry;
+                        p.delta[o] = sD[hh][u];
+                    }
+                    carry += sTail[u0 >> 5][hh];
+                }
+            }
+            __syncthreads();  // the staging arrays are reused by the next piece
+        }
+    }
+    // B and C -> fp16, grid-stride over 16-byte units, four of each in flight per thread
+    const int c0 = (int)gridDim.x > p.nscan ? p.nscan : 0;  // the first converting CTA
+    if ((int)blockIdx.x >= c0) {
         const size_t cnt = (size_t)p.T * p.row16;
-        const size_t stride = (size_t)(gridDim.x - p.nscan) * kPrepThreads;
-        size_t i = (size_t)(blockIdx.x - p.nscan) * kPrepThreads + threadIdx.x;
+        const size_t stride = (size_t)(gridDim.x - c0) * kPrepThreads;
+        size_t i = (size_t)(blockIdx.x - c0) * kPrepThreads + threadIdx.x;
         for (; i + 3 * stride < cnt; i += 4 * stride) {
             uint4 b[4], c[4];
 #pragma unroll
@@ -946,55 +1001,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
             p.Bh[i] = bf16x8_to_f16x8(p.B[i]);
             p.Ch[i] = bf16x8_to_f16x8(p.C[i]);
         }
-        return;
-    }
-    const int nhb = (p.H + 31) / 32;
-    const int hb = blockIdx.x % nhb;
-    const int km = blockIdx.x / nhb;
-    const int k = km / p.mpc, m0 = km - k * p.mpc;
-    const int cs = p.cu_chunk[k], ce = p.cu_chunk[k + 1];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = hb * 32 + lane;
-    const bool hv = h < p.H;
-    const float Ah = hv ? p.A[h] : 0.f;
-    const float bias = (hv && p.dt_bias) ? p.dt_bias[h] : 0.f;
-    const __nv_bfloat16 *dth = p.dt + (hv ? h : 0);
-    for (int tb = cs + 128 * m0; tb < ce; tb += 128 * p.mpc) {
-        const int L = min(128, ce - tb);
-        const int ta = tb + 32 * warp;
-        const int mw = max(0, min(32, tb + L - ta));  // this warp's tokens
-        float dv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) dv[j] = j < mw ? __bfloat162float(dth[(size_t)(ta + j) * p.H]) : 0.f;
-        float run = 0.f;  // the cumsum within this warp's 32 tokens
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (j < mw) {
-                const float d = fast_delta(dv[j] + bias, p.dt_softplus, p.dt_min, p.dt_max);
-                run = fmaf(d, Ah, run);
-                sC[lane][32 * warp + j] = run;
-                sD[lane][32 * warp + j] = d;
-            }
-        }
-        sTail[warp][lane] = run;
-        __syncthreads();
-        // coalesced stores: warp w writes heads w, w + 4, ...; a token adds the totals of the
-        // 32-token quarters before its own
-        for (int hh = warp; hh < 32; hh += 4) {
-            const int h2 = hb * 32 + hh;
-            if (h2 >= p.H) break;
-            float carry = 0.f;
-            for (int u0 = 0; u0 < L; u0 += 32) {
-                const int u = u0 + lane;
-                if (u < L) {
-                    const size_t o = (size_t)h2 * p.T + tb + u;
-                    p.cum[o] = sC[hh][u] + carry;
-                    p.delta[o] = sD[hh][u];
-                }
-                carry += sTail[u0 >> 5][hh];
-            }
-        }
-        __syncthreads();  // the staging arrays are reused by the next piece
     }
 }
 
@@ -1071,7 +1077,9 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
         const int sms = std::max(sm_count(), 1);
         const size_t conv = std::min<size_t>(((size_t)a.total_tokens * q.row16 + 4 * kPrepThreads - 1) / (4 * kPrepThreads),
                                              (size_t)sms * 8);
-        prep_kernel<<<(unsigned)(q.nscan + std::max<size_t>(conv, 1)), kPrepThreads, 0, s>>>(q);
+        // large calls: the scan CTAs also do the conversion; small ones: conversion CTAs of their own
+        const size_t grid = (size_t)q.nscan >= conv ? (size_t)q.nscan : q.nscan + std::max<size_t>(conv, 1);
+        prep_kernel<<<(unsigned)std::max<size_t>(grid, 1), kPrepThreads, 0, s>>>(q);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
