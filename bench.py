@@ -86,7 +86,7 @@ def _sm_max_mhz():
 # 286,149,120 B written; ssd_prefill_tc_kernel 1,422,029,056 B read + 2,092,092,416 B written.  Scaled by
 # tokens (x, y, B/C, delta and one state per 256-token chunk all grow with them).  Only for that head
 # configuration and this kernel version; the summary is in profiles/.
-PREFILL_TRAFFIC_PER_TOKEN = (285256704 + 286660352 + 1423174656 + 2090718208) / 65536
+PREFILL_TRAFFIC_PER_TOKEN = (285269504 + 286591488 + 1424121344 + 2090929408) / 65536
 PREFILL_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of prep_kernel and ssd_prefill_tc_kernel "
                           "on 8 x 8192 tokens, scaled by tokens")
 SM_MAX_MHZ = 2070.0  # GB300's maximum SM clock, where the measured-peaks file does not give it
