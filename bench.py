@@ -222,12 +222,10 @@ class Step:
                              p["cache"], p["D"], p["dt_bias"], chunk_size=p["chunk_size"], seq_order=m["seq_order"])
         self.workspace = torch.empty(max(ssd.ssd_prefill_workspace_size(a), 1), dtype=torch.uint8, device=dev)
         self.prefill_kernels = ssd.ssd_prefill_kernel_count(a)
-        # The mixed step runs the prefill on a high-priority stream and the decode on a
-        # normal-priority one.  A prefill CTA needs a whole SM (shared memory, TMEM), so pending
-        # prefill CTAs take every SM that frees up first; decode CTAs fill the SMs the prefill's
-        # last, partial wave leaves idle.
-        self.hi = torch.cuda.Stream(device=dev, priority=-5)
-        self.side = torch.cuda.Stream(device=dev, priority=0)
+        # The timed steps are issued on a stream of their own (not the legacy default stream,
+        # which would serialise with every other stream); ssd_mixed_step forks the two parts of a
+        # mixed step onto the library's own prioritised streams and joins them back into it.
+        self.stream = torch.cuda.Stream(device=dev)
 
     def metadata(self):
         p = self.pre
@@ -254,7 +252,7 @@ class Step:
     def run(self, ev=None, host=None, mixed=False, bufs=None):
         """One step on the current stream.  ev: optional (start, mid, end) CUDA events around
         the prefill and decode calls (serial step only).  host: pinned host buffers for the e2e
-        leg.  mixed: the decode runs on the side stream beside the prefill (see __init__).
+        leg.  mixed: both calls as one ssd_mixed_step (the decode beside the prefill).
         bufs: another set of device token buffers (x, dt, B, C of both calls and the outputs)."""
         p, d = dict(self.pre), dict(self.dec)
         y, yd = self.y, self.yd
@@ -262,35 +260,32 @@ class Step:
             for name in ("x", "dt", "B", "C"):
                 p[name], d[name] = bufs["p_" + name], bufs["d_" + name]
             y, yd = bufs["y"], bufs["yd"]
-        main = torch.cuda.current_stream()
         if host is not None:  # end to end: this step's inputs come from host memory
             for name in ("x", "dt", "B", "C"):
                 p[name].copy_(host["p_" + name], non_blocking=True)
                 d[name].copy_(host["d_" + name], non_blocking=True)
         meta = self.metadata()
         m = self.device_meta(meta)
-        ready = None
-        if mixed:
-            ready = torch.cuda.Event()
-            ready.record(main)  # inputs and metadata are in place
-        if ev is not None:
-            ev[0].record()
-        self.ssd.ssd_prefill_varlen(p["x"], p["dt"], p["A"], p["B"], p["C"], self.cu_dev, m["cu_chunk_seqlens"],
-                                    m["seq_idx"], m["last_chunk_indices"], out=y, init_slot=m["init_slot"],
-                                    chunk_slot=m["chunk_slot"], state_cache=p["cache"], D=p["D"],
-                                    dt_bias=p["dt_bias"], null_block_id=p["null_block_id"],
-                                    chunk_size=p["chunk_size"], workspace=self.workspace, seq_order=m["seq_order"])
-        if ev is not None:
-            ev[1].record()
-        if self.dec["live"] > 0:
-            if mixed:
-                self.side.wait_event(ready)
-                with torch.cuda.stream(self.side):
-                    self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
-                                               out=yd, D=d["D"], dt_bias=d["dt_bias"],
-                                               null_block_id=d["null_block_id"])
-                main.wait_stream(self.side)
-            else:
+        if mixed and self.dec["live"] > 0:  # both parts in one library call (ssd_mixed_step)
+            pa = self.ssd.prefill_args(p["x"], p["dt"], p["A"], p["B"], p["C"], self.cu_dev, m["cu_chunk_seqlens"],
+                                       m["seq_idx"], m["last_chunk_indices"], y, m["init_slot"], m["chunk_slot"],
+                                       p["cache"], p["D"], p["dt_bias"], null_block_id=p["null_block_id"],
+                                       chunk_size=p["chunk_size"], seq_order=m["seq_order"])
+            da = self.ssd.decode_args(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, yd,
+                                      D=d["D"], dt_bias=d["dt_bias"], null_block_id=d["null_block_id"])
+            self.ssd.ssd_mixed_step(pa, da, workspace=self.workspace)
+        else:
+            if ev is not None:
+                ev[0].record()
+            self.ssd.ssd_prefill_varlen(p["x"], p["dt"], p["A"], p["B"], p["C"], self.cu_dev,
+                                        m["cu_chunk_seqlens"], m["seq_idx"], m["last_chunk_indices"], out=y,
+                                        init_slot=m["init_slot"], chunk_slot=m["chunk_slot"],
+                                        state_cache=p["cache"], D=p["D"], dt_bias=p["dt_bias"],
+                                        null_block_id=p["null_block_id"], chunk_size=p["chunk_size"],
+                                        workspace=self.workspace, seq_order=m["seq_order"])
+            if ev is not None:
+                ev[1].record()
+            if self.dec["live"] > 0:
                 self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
                                            out=yd, D=d["D"], dt_bias=d["dt_bias"],
                                            null_block_id=d["null_block_id"])
@@ -713,7 +708,7 @@ def gpu_arm(args, rank, world, dist_on):
     pre_bytes = prefill_bytes(T, st.K, H, P, N, G, 2)
     dec_bytes = decode_bytes(R, 1, R, H, P, N, G, 2)
     mixed = not args.serial_step
-    torch.cuda.set_stream(st.hi)  # every timed step is issued on the high-priority stream
+    torch.cuda.set_stream(st.stream)
     for _ in range(args.warmup):
         st.run(mixed=mixed)
         st.run()
@@ -770,7 +765,8 @@ def gpu_arm(args, rank, world, dist_on):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded randn tokens, -exp(U(0,2)) A, U(-4,-1) dt_bias)",
         "config": dict(wl, parallelism="dp%d (independent replicas)" % world,
-                       step="prefill on a high-priority stream, decode beside it on a normal-priority one"
+                       step="ssd_mixed_step: prefill on the library's high-priority stream, decode beside it on its "
+                       "low-priority one, started once the prefill's prep kernel is done"
                        if mixed else "prefill then decode on one stream", host_numa_node=numa),
         "prefill": {"tokens_per_s_per_layer": T / (pre_mean * 1e-3), "ms": pre_mean,
                     "algorithmic_bytes": pre_bytes,

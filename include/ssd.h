@@ -326,6 +326,44 @@ typedef struct ssm_decode_args {
 SSD_API ssd_status_t ssm_decode_update(const ssm_decode_args *args, ssd_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * One step of a mixed batch (device)
+ *
+ * A scheduled batch holds prefill requests and decode requests, each part
+ * with its own metadata and state indices ("BaseMambaAttentionMetadata" on
+ * the Mamba (SSM) page: num_prefills / num_decodes, state_indices_tensor_p /
+ * _d; "왜 이 설계인가" item 2: the two parts go to different kernels).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * ssd_mixed_step -- the prefill part and the decode part of one step, issued
+ * together.  The result is that of ssd_prefill_varlen(prefill, workspace,
+ * workspace_bytes, stream) followed by ssm_decode_update(decode, stream),
+ * provided the two parts touch disjoint memory: no state slot that one part
+ * reads or writes is written by the other, and their outputs do not overlap
+ * (err_word may be the same word).  Either part may be empty
+ * (total_tokens == 0 or batch == 0); then this is the other call alone.
+ *
+ * How it runs: the prefill on a library-owned stream of the device's greatest
+ * priority, the decode on one of its least, both forked from `stream` and
+ * joined back into it by events, so that work queued on `stream` later waits
+ * for both.  On the tensor-core path the decode starts once the prefill's
+ * prep kernel is done, so the two bandwidth-bound kernels do not share HBM;
+ * it then gets the SMs that the fused prefill kernel leaves idle (a prefill
+ * CTA needs a whole SM, and pending prefill CTAs, at the greater priority,
+ * take every SM that frees up first), chiefly beside the prefill's last,
+ * partial wave.  On the CUDA-core path the decode starts at once.
+ *
+ * Host checks are those of the two calls, all made before anything is
+ * queued.  The streams and events are made on the first call in each context
+ * (make it before any stream capture) and kept until the process exits; a
+ * device reset makes the next call create them anew.  Calls from several host
+ * threads queue their work one call at a time.  Returns SSD_ERR_CUDA if a
+ * launch or a stream or event operation fails.
+ */
+SSD_API ssd_status_t ssd_mixed_step(const ssd_prefill_args *prefill, void *workspace, size_t workspace_bytes,
+                                    const ssm_decode_args *decode, ssd_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Depthwise causal conv1d before the SSM (device)
  *
  * The step that produces x, B and C: "get hidden_states, B and C after

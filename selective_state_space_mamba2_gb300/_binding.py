@@ -22,7 +22,8 @@ DEVERR_SLOT, DEVERR_METADATA, DEVERR_COLUMN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1
 
 EXPORTED_SYMBOLS = ("ssd_status_string", "ssd_abi_version", "ssd_max_chunks", "ssd_chunk_metadata",
                     "ssd_prefill_workspace_size", "ssd_prefill_kernel_count", "ssd_prefill_varlen",
-                    "ssd_prefill_varlen_noalloc", "ssm_decode_update", "ssd_conv1d_varlen", "ssd_conv1d_update",
+                    "ssd_prefill_varlen_noalloc", "ssm_decode_update", "ssd_mixed_step", "ssd_conv1d_varlen",
+                    "ssd_conv1d_update",
                     "mamba1_scan_varlen", "mamba1_state_update")
 
 _vp = ctypes.c_void_p
@@ -111,6 +112,9 @@ def lib():
         L.ssd_prefill_varlen_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
         L.ssm_decode_update.restype = ctypes.c_int
         L.ssm_decode_update.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        L.ssd_mixed_step.restype = ctypes.c_int
+        L.ssd_mixed_step.argtypes = [ctypes.POINTER(PrefillArgs), _vp, ctypes.c_size_t,
+                                     ctypes.POINTER(DecodeArgs), _vp]
         for fn in ("mamba1_scan_varlen", "mamba1_state_update"):
             getattr(L, fn).restype = ctypes.c_int
             getattr(L, fn).argtypes = [ctypes.POINTER(Mamba1Args), _vp]
@@ -330,6 +334,21 @@ def ssm_decode_update(x, dt, A, B, C, state_cache, state_indices, num_accepted_t
     if rc != SSD_OK:
         raise SSDError("ssm_decode_update", rc)
     return out
+
+
+def ssd_mixed_step(prefill, decode, workspace=None, stream=None):
+    """One step of a mixed batch: ``prefill`` (from :func:`prefill_args`) and ``decode`` (from
+    :func:`decode_args`) issued together on ``stream``; the tensors the two argument sets point
+    to must stay alive until the step is done.  ``workspace`` as for :func:`ssd_prefill_varlen`
+    (allocated with torch when omitted)."""
+    if workspace is None:
+        need = ssd_prefill_workspace_size(prefill) if prefill.total_tokens > 0 else 0
+        dev = torch.device("cuda", torch.cuda.current_device())
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    rc = lib().ssd_mixed_step(ctypes.byref(prefill), ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                              ctypes.byref(decode), _stream(stream))
+    if rc != SSD_OK:
+        raise SSDError("ssd_mixed_step", rc)
 
 
 def conv1d_args(xbc, weight, dim_x, dim_bc, x_out, B_out, C_out, bias=None, conv_state=None, activation="silu",

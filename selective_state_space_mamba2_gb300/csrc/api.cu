@@ -1,6 +1,7 @@
 // C-ABI entry points: host-side argument checks, workspace carving, dispatch.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -66,28 +67,9 @@ extern "C" int32_t ssd_prefill_kernel_count(const ssd_prefill_args *a) {
     return ssd::tc_prefill_supported(*a) ? (ssd::tc_prefill_segments(*a) > 1 ? 3 : 2) : 4;
 }
 
-extern "C" ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *a, void *workspace,
-                                           size_t workspace_bytes, ssd_stream_t stream) {
-    const ssd_status_t st = check_prefill(a);
-    if (st != SSD_OK || a->total_tokens == 0) return st;
-    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    // bf16 with headdim 64 and dstate 128: the fused tensor-core kernel
-    if (ssd::tc_prefill_supported(*a)) {
-        if (!workspace || workspace_bytes < ssd::tc_prefill_workspace(*a) ||
-            (reinterpret_cast<uintptr_t>(workspace) & 255u))
-            return SSD_ERR_WORKSPACE;
-        return from_cuda(ssd::tc_prefill_launch(*a, workspace, cs));
-    }
-    if (!ssd::simt_prefill_supported(*a)) return SSD_ERR_UNSUPPORTED;
-    const size_t need = ssd::simt_prefill_workspace(*a, nullptr, nullptr);
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return SSD_ERR_WORKSPACE;
-    ssd::PrefillWorkspace ws;
-    ssd::simt_prefill_workspace(*a, &ws, workspace);
-    return from_cuda(ssd::simt_prefill_launch(*a, ws, cs));
-}
+namespace {
 
-extern "C" ssd_status_t ssm_decode_update(const ssm_decode_args *a, ssd_stream_t stream) {
+ssd_status_t check_decode(const ssm_decode_args *a) {
     if (!a) return SSD_ERR_INVALID_ARG;
     if (a->batch < 0 || a->tokens_per_req < 1 || a->state_indices_cols < a->tokens_per_req)
         return SSD_ERR_INVALID_ARG;
@@ -99,7 +81,123 @@ extern "C" ssd_status_t ssm_decode_update(const ssm_decode_args *a, ssd_stream_t
         return SSD_ERR_INVALID_ARG;
     if (!aligned16(a->state_cache) || a->dstate % 4 != 0) return SSD_ERR_INVALID_ARG;
     if (!ssd::decode_supported(*a)) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+// The prefill's workspace check and launch; after_prep as for tc_prefill_launch (recorded only
+// on the tensor-core path).
+ssd_status_t prefill_checked_launch(const ssd_prefill_args *a, void *workspace, size_t workspace_bytes,
+                                    cudaStream_t cs, cudaEvent_t after_prep) {
+    // bf16 with headdim 64 and dstate 128: the fused tensor-core kernel
+    if (ssd::tc_prefill_supported(*a)) {
+        if (!workspace || workspace_bytes < ssd::tc_prefill_workspace(*a) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return SSD_ERR_WORKSPACE;
+        return from_cuda(ssd::tc_prefill_launch(*a, workspace, cs, after_prep));
+    }
+    if (!ssd::simt_prefill_supported(*a)) return SSD_ERR_UNSUPPORTED;
+    const size_t need = ssd::simt_prefill_workspace(*a, nullptr, nullptr);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SSD_ERR_WORKSPACE;
+    ssd::PrefillWorkspace ws;
+    ssd::simt_prefill_workspace(*a, &ws, workspace);
+    return from_cuda(ssd::simt_prefill_launch(*a, ws, cs));
+}
+
+// ssd_mixed_step's streams and events, one set per device, made in the context current at the
+// time and made again when a later call finds another context there (after a device reset).
+struct MixedSet {
+    void *ctx = nullptr;
+    cudaStream_t hi = nullptr, lo = nullptr;  // prefill (greatest priority), decode (least)
+    cudaEvent_t fork = nullptr, prep = nullptr, hi_done = nullptr, lo_done = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_mixed_mutex;  // held from the lookup to the last event of a call
+MixedSet g_mixed[kMaxDevices];
+
+cudaError_t mixed_set(MixedSet **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    e = cudaFree(nullptr);  // makes the device's primary context current if it is not yet
+    if (e != cudaSuccess) return e;
+    void *ctx = nullptr;
+    if (!ssd::current_context(&ctx) || !ctx) return cudaErrorDeviceUninitialized;
+    MixedSet &m = g_mixed[dev];
+    if (m.ctx != ctx) {  // first call here, or the old context is gone: its handles went with it
+        MixedSet n;
+        int least = 0, greatest = 0;
+        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&n.hi, cudaStreamNonBlocking, greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&n.lo, cudaStreamNonBlocking, least);
+        for (cudaEvent_t *ev : {&n.fork, &n.prep, &n.hi_done, &n.lo_done})
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+        n.ctx = ctx;
+        m = n;
+    }
+    *out = &m;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *a, void *workspace,
+                                           size_t workspace_bytes, ssd_stream_t stream) {
+    const ssd_status_t st = check_prefill(a);
+    if (st != SSD_OK || a->total_tokens == 0) return st;
+    return prefill_checked_launch(a, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" ssd_status_t ssm_decode_update(const ssm_decode_args *a, ssd_stream_t stream) {
+    const ssd_status_t st = check_decode(a);
+    if (st != SSD_OK || a->batch == 0) return st;
     return from_cuda(ssd::decode_launch(*a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" ssd_status_t ssd_mixed_step(const ssd_prefill_args *prefill, void *workspace, size_t workspace_bytes,
+                                       const ssm_decode_args *decode, ssd_stream_t stream) {
+    ssd_status_t st = check_prefill(prefill);
+    if (st != SSD_OK) return st;
+    st = check_decode(decode);
+    if (st != SSD_OK) return st;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const bool has_prefill = prefill->total_tokens > 0, has_decode = decode->batch > 0;
+    if (has_prefill && !ssd::tc_prefill_supported(*prefill) && !ssd::simt_prefill_supported(*prefill))
+        return SSD_ERR_UNSUPPORTED;
+    if (has_prefill) {
+        const size_t need = ssd::tc_prefill_supported(*prefill) ? ssd::tc_prefill_workspace(*prefill)
+                                                                : ssd::simt_prefill_workspace(*prefill, nullptr, nullptr);
+        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return SSD_ERR_WORKSPACE;
+    }
+    if (!has_decode) return has_prefill ? prefill_checked_launch(prefill, workspace, workspace_bytes, cs, nullptr) : SSD_OK;
+    if (!has_prefill) return from_cuda(ssd::decode_launch(*decode, cs));
+
+    std::lock_guard<std::mutex> lock(g_mixed_mutex);
+    MixedSet *m = nullptr;
+    cudaError_t e = mixed_set(&m);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    // fork: both streams start after the work queued on `stream` so far
+    e = cudaEventRecord(m->fork, cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(m->hi, m->fork, 0);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    // The decode starts once the prefill's prep kernel is done: the CUDA-core path records
+    // nothing there, so it waits for the fork alone (recorded again on hi for the same effect).
+    e = cudaEventRecord(m->prep, m->hi);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
+    st = prefill_checked_launch(prefill, workspace, workspace_bytes, m->hi, m->prep);
+    // join the hi stream back even when the prefill failed to launch, so that `stream` is left
+    // ordered after whatever did get queued
+    e = cudaStreamWaitEvent(m->lo, m->prep, 0);
+    if (e == cudaSuccess && st == SSD_OK) e = ssd::decode_launch(*decode, m->lo);
+    cudaError_t j = cudaEventRecord(m->hi_done, m->hi);
+    if (j == cudaSuccess) j = cudaEventRecord(m->lo_done, m->lo);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(cs, m->hi_done, 0);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(cs, m->lo_done, 0);
+    if (st != SSD_OK) return st;
+    return e == cudaSuccess && j == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 namespace {

@@ -88,7 +88,10 @@ bool simt_prefill_supported(const ssd_prefill_args &a);
 bool tc_prefill_supported(const ssd_prefill_args &a);
 int tc_prefill_segments(const ssd_prefill_args &a);
 size_t tc_prefill_workspace(const ssd_prefill_args &a);
-cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s);
+// after_prep: recorded on s once the prep kernel is queued (before the segment pass and the
+// fused kernel), or nullptr
+cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s,
+                              cudaEvent_t after_prep = nullptr);
 
 bool decode_supported(const ssm_decode_args &a);
 cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s);
@@ -96,4 +99,8 @@ cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s);
 cudaError_t conv1d_launch(const ssd_conv1d_args &a, bool decode, cudaStream_t s);
 
 cudaError_t mamba1_launch(const mamba1_args &a, bool decode, cudaStream_t s);
+
+// The current context (CUcontext) as an opaque handle: false when the driver entry point is
+// unavailable; *ctx is null until the runtime has made a context current on this thread.
+bool current_context(void **ctx);
 }  // namespace ssd

@@ -19,22 +19,8 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BY
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-CUcontext g_scratch_ctx[kMaxDevices];  // context the address below was looked up in
+void *g_scratch_ctx[kMaxDevices];      // context the address below was looked up in
 void *g_scratch_addr[kMaxDevices];     // device address of g_noalloc_scratch, per device ordinal
-
-// cuCtxGetCurrent, reached through the runtime (the library does not link the driver itself)
-using CtxGetCurrentFn = CUresult (*)(CUcontext *);
-CtxGetCurrentFn ctx_get_current() {
-    static CtxGetCurrentFn fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<CtxGetCurrentFn>(p);
-    }
-    return fn;
-}
 
 // Device address of the scratch array on the current device.  The name of a
 // __device__ variable is only a host-side stand-in, so its address is asked
@@ -46,16 +32,14 @@ cudaError_t scratch_on_current_device(void **addr) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    const CtxGetCurrentFn get_ctx = ctx_get_current();
-    if (!get_ctx) return cudaErrorDeviceUninitialized;
-    CUcontext ctx = nullptr;  // null until the runtime has made the device's context current
-    if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    void *ctx = nullptr;  // null until the runtime has made the device's context current
+    if (!ssd::current_context(&ctx)) return cudaErrorDeviceUninitialized;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!ctx || !g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // sets the primary context up if needed
         if (e != cudaSuccess) return e;
-        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+        if (!ssd::current_context(&ctx) || !ctx) return cudaErrorDeviceUninitialized;
         g_scratch_addr[dev] = p;
         g_scratch_ctx[dev] = ctx;
     }
@@ -64,6 +48,25 @@ cudaError_t scratch_on_current_device(void **addr) {
 }
 
 }  // namespace
+
+namespace ssd {
+// cuCtxGetCurrent, reached through the runtime (the library does not link the driver itself)
+bool current_context(void **ctx) {
+    using Fn = CUresult (*)(CUcontext *);
+    static Fn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                       q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<Fn>(p)
+                   : nullptr;
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return false;
+    *ctx = c;
+    return true;
+}
+}  // namespace ssd
 
 extern "C" ssd_status_t ssd_prefill_varlen_noalloc(const ssd_prefill_args *a, ssd_stream_t stream) {
     // the same host checks as ssd_prefill_varlen, through its public size query

@@ -1044,7 +1044,7 @@ bool tc_prefill_supported(const ssd_prefill_args &a) {
     return a.dtype == SSD_BF16 && a.headdim == kP && a.dstate == kN && a.total_tokens > 0;
 }
 
-cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s) {
+cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s, cudaEvent_t after_prep) {
     CUtensorMap mX, mB, mC, mY;
     const uint64_t T = (uint64_t)a.total_tokens;
     const size_t bc = (size_t)a.total_tokens * a.ngroups * kN * 2;
@@ -1081,6 +1081,7 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
         const size_t grid = (size_t)q.nscan >= conv ? (size_t)q.nscan : q.nscan + std::max<size_t>(conv, 1);
         prep_kernel<<<(unsigned)std::max<size_t>(grid, 1), kPrepThreads, 0, s>>>(q);
         cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess && after_prep) e = cudaEventRecord(after_prep, s);
         if (e != cudaSuccess) return e;
     }
     if (!make_tmap_bf16_3d(&mX, a.x, kP, a.nheads, T, (uint64_t)kP * 2, (uint64_t)a.nheads * kP * 2, 64, 1, kL) ||

@@ -195,6 +195,32 @@ def test_empty_decode_is_a_no_op(lib):
     assert lib.ssm_decode_update(ctypes.byref(a), None) == B.SSD_OK
 
 
+@pytest.mark.parametrize("pre,dec,code", [
+    (dict(ngroups=3), {}, B.SSD_ERR_INVALID_ARG),       # a bad prefill part
+    ({}, dict(tokens_per_req=0), B.SSD_ERR_INVALID_ARG),  # a bad decode part
+    ({}, dict(dstate=12), B.SSD_ERR_UNSUPPORTED),
+    (dict(headdim=257), dict(batch=0), B.SSD_ERR_INVALID_ARG),  # checked even beside an empty part
+    (dict(total_tokens=0, num_chunks=0), dict(state_cache=0x10004), B.SSD_ERR_INVALID_ARG),
+])
+def test_mixed_step_checks_both_parts_before_queueing(lib, pre, dec, code):
+    """ssd_mixed_step makes the host checks of both calls before anything is queued, so a bad
+    part is refused on a machine without a GPU."""
+    a, d = _prefill_args(**pre), _decode_args(**dec)
+    assert lib.ssd_mixed_step(ctypes.byref(a), None, 0, ctypes.byref(d), None) == code
+
+
+def test_mixed_step_refuses_a_short_workspace_before_queueing(lib):
+    a, d = _prefill_args(), _decode_args()
+    need = lib.ssd_prefill_workspace_size(ctypes.byref(a))
+    assert lib.ssd_mixed_step(ctypes.byref(a), ctypes.c_void_p(0x100000), need - 1, ctypes.byref(d), None) \
+        == B.SSD_ERR_WORKSPACE
+
+
+def test_empty_mixed_step_is_a_no_op(lib):
+    a, d = _prefill_args(total_tokens=0, num_chunks=0), _decode_args(batch=0)
+    assert lib.ssd_mixed_step(ctypes.byref(a), None, 0, ctypes.byref(d), None) == B.SSD_OK
+
+
 def _conv_args(**over):
     a = B.Conv1dArgs()
     a.total_tokens, a.num_seqs, a.num_chunks, a.tokens_per_req = 8, 2, 0, 4
