@@ -3,6 +3,7 @@ the fp64 oracle, and bit for bit against the two calls made one after the other.
 import ctypes
 import math
 
+import numpy as np
 import pytest
 import torch
 
@@ -160,3 +161,39 @@ def test_decode_beside_a_tensor_core_prefill(P, tpr):
     e_yd, e_sd, ok, tol_d, nlive = PT.check_decode(dec, yd, before_d, dec["cache"])
     assert nlive == 11 and ok and e_yd <= tol_d and e_sd <= tol_d, (e_yd, e_sd)
     del keep, na, si
+
+
+def test_long_mixed_step_full_size_sampled():
+    """The benchmark's step at full size, in the configuration it is timed in (one ssd_mixed_step
+    call): 8 x 65536 prefill tokens and 384 decodes on a 16384-slot cache.  y and all 2048 chunk
+    states on two heads, six decode requests in full, fingerprints of every slot neither part
+    writes."""
+    pre, dec = W.long_mixed(DEV)
+    cache = pre["cache"]
+    reqs = [0, 1, 77, 200, 301, 383]
+    read_before = {int(dec["state_indices"][r, 0]): cache[int(dec["state_indices"][r, 0])].clone() for r in reqs}
+    fp_before = PT.slot_fingerprints(cache)
+    meta = PT.prefill_metadata(pre)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = torch.empty_like(pre["x"])
+    yd = torch.full_like(dec["x"], float("nan"))
+    pa, da, keep = _args(pre, dec, meta, y, yd, err)
+    ssd.ssd_mixed_step(pa, da)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    heads = [3, 126]
+    yo, cso = PT.oracle_prefill(pre, meta, cache, heads=heads)
+    hs = torch.tensor(heads)
+    tol = PT.TOL[torch.bfloat16]
+    assert PT.y_err(y[:, hs].double().cpu().numpy(), yo, torch.bfloat16) <= tol
+    sl = torch.from_numpy(meta["chunk_slot"].astype(np.int64)).to(DEV)
+    assert PT.rel_err(cache[sl][:, hs].double().cpu().numpy(), cso) <= tol
+    e_yd, e_sd, _, tol_d, nlive = PT.check_decode(dec, yd, read_before, cache, requests=reqs, check_untouched=False)
+    assert nlive == len(reqs) and e_yd <= tol_d and e_sd <= tol_d, (e_yd, e_sd)
+    assert not torch.isnan(yd).any()  # every decode row written
+    fp_after = PT.slot_fingerprints(cache)
+    mask = torch.ones_like(fp_after, dtype=torch.bool)
+    mask[sl] = False
+    mask[dec["state_indices"][:, 0].long().to(DEV)] = False
+    assert torch.equal(fp_after[mask], fp_before[mask])
+    del keep
