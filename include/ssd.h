@@ -356,7 +356,9 @@ SSD_API ssd_status_t ssm_decode_update(const ssm_decode_args *args, ssd_stream_t
  * Host checks are those of the two calls, all made before anything is
  * queued.  The streams and events are made on the first call in each context
  * (make it before any stream capture) and kept until the process exits; a
- * device reset makes the next call create them anew.  Calls from several host
+ * device reset makes the next call create them anew.  After that first call
+ * the step can be captured into a CUDA graph on `stream`: the fork onto the
+ * library's streams and the join back are captured with it.  Calls from several host
  * threads queue their work one call at a time.  Returns SSD_ERR_CUDA if a
  * launch or a stream or event operation fails.
  */

@@ -120,10 +120,13 @@ cudaError_t mixed_set(MixedSet **out) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    e = cudaFree(nullptr);  // makes the device's primary context current if it is not yet
-    if (e != cudaSuccess) return e;
     void *ctx = nullptr;
-    if (!ssd::current_context(&ctx) || !ctx) return cudaErrorDeviceUninitialized;
+    if (!ssd::current_context(&ctx)) return cudaErrorDeviceUninitialized;
+    if (!ctx) {  // no context current on this thread yet: make the device's primary one current
+        e = cudaFree(nullptr);
+        if (e != cudaSuccess) return e;
+        if (!ssd::current_context(&ctx) || !ctx) return cudaErrorDeviceUninitialized;
+    }
     MixedSet &m = g_mixed[dev];
     if (m.ctx != ctx) {  // first call here, or the old context is gone: its handles went with it
         MixedSet n;

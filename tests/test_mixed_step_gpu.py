@@ -197,3 +197,45 @@ def test_long_mixed_step_full_size_sampled():
     mask[dec["state_indices"][:, 0].long().to(DEV)] = False
     assert torch.equal(fp_after[mask], fp_before[mask])
     del keep
+
+
+def test_mixed_step_replays_as_a_graph():
+    """Captured once (after an eager call has made the library's streams and events) and replayed
+    with new token contents and states, the step gives the bits of an eager call on the same
+    inputs: the fork onto the library's streams and the join back are captured with it."""
+    pre, dec = _case(3, 900, 64, num_decodes=24, seed=91)
+    cache = pre["cache"]
+    meta = PT.prefill_metadata(pre)
+    y = torch.full_like(pre["x"], float("nan"))
+    yd = torch.full_like(dec["x"], float("nan"))
+    pa, da, keep = _args(pre, dec, meta, y, yd, None)
+    ws = torch.empty(max(ssd.ssd_prefill_workspace_size(pa), 1), dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ssd.ssd_mixed_step(pa, da, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ssd.ssd_mixed_step(pa, da, workspace=ws)
+    g = torch.Generator(device=DEV).manual_seed(92)
+    for _ in range(2):
+        for t in (pre["x"], pre["B"], pre["C"], dec["x"], dec["B"], dec["C"]):
+            t.copy_(torch.randn(t.shape, generator=g, device=DEV).to(t.dtype))
+        before = cache.clone()
+        y.fill_(float("nan"))
+        yd.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = (y.clone(), yd.clone(), cache.clone())
+        cache.copy_(before)
+        y.fill_(float("nan"))
+        yd.fill_(float("nan"))
+        ssd.ssd_mixed_step(pa, da, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got[0].view(torch.int16), y.view(torch.int16))
+        assert torch.equal(got[1].view(torch.int16), yd.view(torch.int16))
+        assert torch.equal(got[2].view(torch.int32), cache.view(torch.int32))
+        assert not torch.isnan(y).any() and not torch.isnan(yd).any()
+    del keep
