@@ -120,6 +120,12 @@ def test_prefill_host_validation(lib, over, code):
     assert lib.ssd_prefill_workspace_size(ctypes.byref(a)) == 0
 
 
+def test_prefill_beyond_the_cuda_core_path_is_unsupported(lib):
+    # headdim x dstate above 16384 (the CUDA-core kernels' per-CTA state), not a tensor-core shape
+    a = _prefill_args(headdim=256, dstate=256)
+    assert lib.ssd_prefill_varlen(ctypes.byref(a), ctypes.c_void_p(0x100000), 1 << 40, None) == B.SSD_ERR_UNSUPPORTED
+
+
 def test_prefill_workspace_too_small_is_refused(lib):
     a = _prefill_args()
     need = lib.ssd_prefill_workspace_size(ctypes.byref(a))

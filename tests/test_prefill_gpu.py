@@ -69,6 +69,15 @@ def test_small_dims_no_D_no_bias_and_dt_limit():
     _run_and_check(case, D=None, dt_bias=None, dt_limit=(0.05, 0.4))
 
 
+@pytest.mark.parametrize("P,N,dtype", [(128, 128, torch.bfloat16), (256, 64, torch.float32), (64, 256, torch.bfloat16)])
+def test_largest_cuda_core_shapes(P, N, dtype):
+    """The CUDA-core path at the largest headdim x dstate it takes (P N = 16384), varlen with
+    initial states and ragged chunks."""
+    case = W.prefill_case(40 + P, [300, 97], [0, 130], 2, P, N, 1, 64, dtype=dtype, device=DEV,
+                          has_init=[False, True], num_slots=24)
+    _run_and_check(case)
+
+
 @pytest.mark.parametrize("with_init", [False, True])
 def test_warmup_shape_single_chunk_2048(with_init):
     """seqlen = chunk_size = 2048, H=48, P=64, N=128, G=4, bf16, with and without initial state."""
