@@ -56,6 +56,18 @@ def test_varlen_ragged_partial_chunks(dtype, null):
     _run_and_check(case)
 
 
+@pytest.mark.parametrize("Q", [96, 200, 384, 1024])
+def test_tensor_core_path_chunk_sizes_off_the_block(Q):
+    """Chunk sizes that are not 128: blocks never cross a chunk end, so chunks of 96 or 200 tokens
+    make every block short, and 384 or 1024 put several blocks in a chunk; with unaligned computed
+    prefixes (partial first chunks), initial states and ragged tails."""
+    new = [700, 5, 333, 1500]
+    nc = [0, 17, Q - 1, 3 * Q + 5]
+    case = W.prefill_case(50 + Q, new, nc, 4, 64, 128, 2, Q, device=DEV, has_init=[False, True, True, True],
+                          num_slots=80)
+    _run_and_check(case)
+
+
 def test_default_mode_one_slot_per_sequence():
     new = [100, 260, 7]
     case = W.prefill_case(12, new, [5, 0, 33], 6, 64, 128, 3, 128, device=DEV,
