@@ -239,3 +239,36 @@ def test_mixed_step_replays_as_a_graph():
         assert torch.equal(got[2].view(torch.int32), cache.view(torch.int32))
         assert not torch.isnan(y).any() and not torch.isnan(yd).any()
     del keep
+
+
+@pytest.mark.parametrize("P", [64, 32])
+def test_mixed_step_with_the_output_gate(P):
+    """Both parts gated (y * silu(z)): the tensor-core prefill's gated instance (headdim 64) or the
+    CUDA-core one (headdim 32), and the decode's."""
+    pre, dec = _case(2, 600, P, num_decodes=12, seed=95 + P)
+    g = torch.Generator(device=DEV).manual_seed(96)
+    zp = torch.randn(pre["x"].shape, generator=g, device=DEV).to(pre["x"].dtype)
+    zd = torch.randn(dec["x"].shape, generator=g, device=DEV).to(dec["x"].dtype)
+    cache = pre["cache"]
+    before = cache.clone()
+    meta = PT.prefill_metadata(pre)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = torch.full_like(pre["x"], float("nan"))
+    yd = torch.full_like(dec["x"], float("nan"))
+    t = {k: torch.from_numpy(v).to(DEV) for k, v in meta.items()}
+    t["cu_seqlens"] = pre["cu_seqlens"].to(DEV)
+    pa = ssd.prefill_args(pre["x"], pre["dt"], pre["A"], pre["B"], pre["C"], t["cu_seqlens"], t["cu_chunk_seqlens"],
+                          t["seq_idx"], t["last_chunk_indices"], y, t["init_slot"], t["chunk_slot"], cache, pre["D"],
+                          pre["dt_bias"], z=zp, null_block_id=pre["null_block_id"], chunk_size=pre["chunk_size"],
+                          err_word=err, seq_order=t.get("seq_order"))
+    si = dec["state_indices"].to(DEV)
+    da = ssd.decode_args(dec["x"], dec["dt"], dec["A"], dec["B"], dec["C"], cache, si, yd, D=dec["D"],
+                         dt_bias=dec["dt_bias"], z=zd, null_block_id=dec["null_block_id"], err_word=err)
+    ssd.ssd_mixed_step(pa, da)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    e_y, e_s, _, tol = PT.check_prefill(pre, y, meta, before, cache, z=zp)
+    assert e_y <= tol and e_s <= tol, (e_y, e_s)
+    e_yd, e_sd, ok, tol_d, nlive = PT.check_decode(dec, yd, before, cache, check_untouched=False, z=zd)
+    assert nlive == 12 and ok and e_yd <= tol_d and e_sd <= tol_d, (e_yd, e_sd)
+    del t, si
