@@ -82,20 +82,23 @@ def _sm_max_mhz():
 # ------------------------------------------------------------- byte counts --
 
 # DRAM traffic of one prefill call (tensor-core path, no segment split), from one ncu capture of both
-# its kernels on 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256: prep_kernel 285,269,760 B read +
-# 286,149,120 B written; ssd_prefill_tc_kernel 1,422,029,056 B read + 2,092,092,416 B written.  Scaled by
+# its kernels on 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256: prep_kernel 285,269,504 B read +
+# 286,591,488 B written; ssd_prefill_tc_kernel 1,424,121,344 B read + 2,090,929,408 B written.  Scaled by
 # tokens (x, y, B/C, delta and one state per 256-token chunk all grow with them).  Only for that head
 # configuration and this kernel version; the summary is in profiles/.
-PREFILL_TRAFFIC_PER_TOKEN = (285269504 + 286591488 + 1424121344 + 2090929408) / 65536
+FUSED_TRAFFIC_PER_TOKEN = (1424121344 + 2090929408) / 65536
+PREFILL_TRAFFIC_PER_TOKEN = (285269504 + 286591488) / 65536 + FUSED_TRAFFIC_PER_TOKEN
 PREFILL_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of prep_kernel and ssd_prefill_tc_kernel "
                           "on 8 x 8192 tokens, scaled by tokens")
+FUSED_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of ssd_prefill_tc_kernel on 8 x 8192 "
+                        "tokens, scaled by tokens")
 SM_MAX_MHZ = 2070.0  # GB300's maximum SM clock, where the measured-peaks file does not give it
 
 
-def prefill_traffic(T, H, P, N, G):
+def prefill_traffic(T, H, P, N, G, fused_only=False):
     if (H, P, N, G) != (128, 64, 128, 8):
         return None
-    return PREFILL_TRAFFIC_PER_TOKEN * T
+    return (FUSED_TRAFFIC_PER_TOKEN if fused_only else PREFILL_TRAFFIC_PER_TOKEN) * T
 
 
 def prefill_bytes(T, K, H, P, N, G, elt, init_reads=0):
@@ -103,6 +106,12 @@ def prefill_bytes(T, K, H, P, N, G, elt, init_reads=0):
     token; one fp32 state store per chunk; one state load per initial state."""
     per_tok = 2 * H * P * elt + H * elt + 2 * G * N * elt
     return T * per_tok + (K + init_reads) * H * P * N * 4
+
+
+def fused_bytes(T, K, H, P, N, G, elt, init_reads=0):
+    """The fused kernel's share of the call's algorithmic bytes: all of them but dt, which the prep
+    kernel reads (the fused kernel reads its delta and cumsum instead)."""
+    return prefill_bytes(T, K, H, P, N, G, elt, init_reads) - T * H * elt
 
 
 # The fused prefill cuts every chunk into blocks of at most 128 tokens and issues, per block and
@@ -250,8 +259,9 @@ class Step:
         return out
 
     def run(self, ev=None, host=None, mixed=False, bufs=None):
-        """One step on the current stream.  ev: optional (start, mid, end) CUDA events around
-        the prefill and decode calls (serial step only).  host: pinned host buffers for the e2e
+        """One step on the current stream.  ev: optional (start, fused, mid, end) CUDA events: before
+        the prefill call, at the library's mark before its fused kernel, between the calls and after
+        the decode (serial step only).  host: pinned host buffers for the e2e
         leg.  mixed: both calls as one ssd_mixed_step (the decode beside the prefill).
         bufs: another set of device token buffers (x, dt, B, C of both calls and the outputs)."""
         p, d = dict(self.pre), dict(self.dec)
@@ -282,15 +292,16 @@ class Step:
                                         init_slot=m["init_slot"], chunk_slot=m["chunk_slot"],
                                         state_cache=p["cache"], D=p["D"], dt_bias=p["dt_bias"],
                                         null_block_id=p["null_block_id"], chunk_size=p["chunk_size"],
-                                        workspace=self.workspace, seq_order=m["seq_order"])
+                                        workspace=self.workspace, seq_order=m["seq_order"],
+                                        mark=None if ev is None else ev[1])
             if ev is not None:
-                ev[1].record()
+                ev[2].record()
             if self.dec["live"] > 0:
                 self.ssd.ssm_decode_update(d["x"], d["dt"], d["A"], d["B"], d["C"], d["cache"], self.si_dev, None,
                                            out=yd, D=d["D"], dt_bias=d["dt_bias"],
                                            null_block_id=d["null_block_id"])
         if ev is not None:
-            ev[2].record()
+            ev[3].record()
         if host is not None:
             host["y"].copy_(y, non_blocking=True)
             host["yd"].copy_(yd, non_blocking=True)
@@ -714,7 +725,7 @@ def gpu_arm(args, rank, world, dist_on):
         st.run()
     torch.cuda.synchronize()
 
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
@@ -736,8 +747,9 @@ def gpu_arm(args, rank, world, dist_on):
         for i in range(args.steps):
             st.run(ev=evs[i])
         torch.cuda.synchronize()
-    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pre_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    fused_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
 
     # end to end: inputs from pinned host memory, y back to host, every step
     e2e_value, e2e_ms, h2d, d2h = None, None, 0, 0
@@ -757,8 +769,11 @@ def gpu_arm(args, rank, world, dist_on):
     pre_flops = prefill_mma_flops(st.meta["cu_chunk_seqlens"], H, P, N)
     method_flops = prefill_method_flops(T, H, P, N, G)
     pre_mean = statistics.mean(pre_ms)
+    fused_mean = statistics.mean(fused_ms)
     dec_mean = statistics.mean(dec_ms) if R > 0 else 0.0
     achieved = pre_bytes / (pre_mean * 1e-3) / 1e9
+    f_bytes = fused_bytes(T, st.K, H, P, N, G, 2)
+    f_achieved = f_bytes / (fused_mean * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -771,16 +786,19 @@ def gpu_arm(args, rank, world, dist_on):
         "prefill": {"tokens_per_s_per_layer": T / (pre_mean * 1e-3), "ms": pre_mean,
                     "algorithmic_bytes": pre_bytes,
                     "hbm_frac": achieved / hbm,
-                    "tensor": {"achieved": pre_flops / (pre_mean * 1e-3) / 1e12, "peak": bf16,
-                               "unit": "TFLOP/s", "frac": pre_flops / (pre_mean * 1e-3) / 1e12 / bf16,
+                    "what": "the whole call (%d kernels): its algorithmic bytes / its time" % st.prefill_kernels,
+                    "fused_kernel_ms": fused_mean, "prep_ms": pre_mean - fused_mean,
+                    "tensor": {"achieved": pre_flops / (fused_mean * 1e-3) / 1e12, "peak": bf16,
+                               "unit": "TFLOP/s", "frac": pre_flops / (fused_mean * 1e-3) / 1e12 / bf16,
                                "flops": pre_flops, "peak_source": bf16_kind,
-                               "what": "tcgen05 flops the fused kernel issues: four products per 128-token "
-                                       "block and head on full tiles, fp16 operands, fp32 accumulators"},
+                               "what": "tcgen05 flops the fused kernel issues (four products per 128-token "
+                                       "block and head on full tiles, fp16 operands, fp32 accumulators) / "
+                                       "the fused kernel's time"},
                     "method_flops": {"flops": method_flops,
-                                     "achieved": method_flops / (pre_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
-                                     "frac": method_flops / (pre_mean * 1e-3) / 1e12 / bf16,
-                                     "what": "G Q N + H Q P + 4 H P N per token at Q = 128: the causal halves "
-                                             "only, C B^T once per group"}},
+                                     "achieved": method_flops / (fused_mean * 1e-3) / 1e12, "unit": "TFLOP/s",
+                                     "frac": method_flops / (fused_mean * 1e-3) / 1e12 / bf16,
+                                     "what": "G Q N + H Q P + 4 H P N per token at Q = 128 (the causal halves "
+                                             "only, C B^T once per group) / the fused kernel's time"}},
         "mixed_step": {"ms": ms_step, "prefill_alone_ms": pre_mean, "decode_alone_ms": dec_mean,
                        "serial_ms": pre_mean + dec_mean,
                        "bound_ms": pre_mean,
@@ -790,11 +808,16 @@ def gpu_arm(args, rank, world, dist_on):
         "decode": {"state_updates_per_s": R / (dec_mean * 1e-3) if R else None, "ms": dec_mean,
                    "algorithmic_bytes": dec_bytes,
                    "hbm_frac": dec_bytes / (dec_mean * 1e-3) / 1e9 / hbm if R else None},
-        "roofline": {"kernel": "ssd_prefill_varlen (%d kernels)" % st.prefill_kernels, "bound": "hbm",
-                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": prefill_traffic(T, H, P, N, G), "traffic_source": PREFILL_TRAFFIC_SOURCE,
-                     "peak_source": peak_kind,
-                     "units": "prefill algorithmic bytes per call / mean call time (CUDA events)"},
+        "roofline": {"kernel": "ssd_prefill_tc_kernel (the fused kernel of ssd_prefill_varlen)", "bound": "hbm",
+                     "achieved": f_achieved, "peak": hbm, "unit": "GB/s", "frac": f_achieved / hbm,
+                     "traffic": prefill_traffic(T, H, P, N, G, fused_only=True),
+                     "traffic_source": FUSED_TRAFFIC_SOURCE, "peak_source": peak_kind,
+                     "algorithmic_bytes": f_bytes, "ms": fused_mean,
+                     "units": "the kernel's algorithmic bytes per launch (the call's, less dt, which the prep "
+                              "kernel reads) / its mean launch time, CUDA events on its stream: one the library "
+                              "records right before the launch (ssd_prefill_varlen_marked), one after the call",
+                     "call": {"kernels": st.prefill_kernels, "achieved": achieved, "frac": achieved / hbm,
+                              "traffic": prefill_traffic(T, H, P, N, G), "traffic_source": PREFILL_TRAFFIC_SOURCE}},
         "clocks": clk.summary(),
         "e2e": None if e2e_ms is None else {"value": e2e_value, "unit": UNIT,
                                             "how": "every step uploads its inputs from pinned host memory and "

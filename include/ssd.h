@@ -245,6 +245,20 @@ SSD_API ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *args, void *work
                                 size_t workspace_bytes, ssd_stream_t stream);
 
 /*
+ * ssd_prefill_varlen_marked -- ssd_prefill_varlen that also records the
+ * caller's CUDA event `event_before_fused` (a cudaEvent_t, or NULL) on
+ * `stream` right before the call's main kernel: on the tensor-core path after
+ * the prep kernel (and the segment pass, when it runs), so that the caller's
+ * own events before the call, at this mark and after the call time the
+ * preparation and the fused kernel apart; on the CUDA-core path before its
+ * first kernel.  Results, checks and errors are those of ssd_prefill_varlen;
+ * a failed record returns SSD_ERR_CUDA.
+ */
+SSD_API ssd_status_t ssd_prefill_varlen_marked(const ssd_prefill_args *args, void *workspace,
+                                               size_t workspace_bytes, ssd_stream_t stream,
+                                               void *event_before_fused);
+
+/*
  * ssd_prefill_varlen_noalloc -- the prefill for callers that cannot allocate.
  *
  * The pages have no counterpart to this call.  It exists for callers that

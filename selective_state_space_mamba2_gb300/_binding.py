@@ -22,7 +22,8 @@ DEVERR_SLOT, DEVERR_METADATA, DEVERR_COLUMN, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1
 
 EXPORTED_SYMBOLS = ("ssd_status_string", "ssd_abi_version", "ssd_max_chunks", "ssd_chunk_metadata",
                     "ssd_prefill_workspace_size", "ssd_prefill_kernel_count", "ssd_prefill_varlen",
-                    "ssd_prefill_varlen_noalloc", "ssm_decode_update", "ssd_mixed_step", "ssd_conv1d_varlen",
+                    "ssd_prefill_varlen_marked", "ssd_prefill_varlen_noalloc", "ssm_decode_update", "ssd_mixed_step",
+                    "ssd_conv1d_varlen",
                     "ssd_conv1d_update",
                     "mamba1_scan_varlen", "mamba1_state_update")
 
@@ -108,6 +109,8 @@ def lib():
         L.ssd_prefill_kernel_count.argtypes = [ctypes.POINTER(PrefillArgs)]
         L.ssd_prefill_varlen.restype = ctypes.c_int
         L.ssd_prefill_varlen.argtypes = [ctypes.POINTER(PrefillArgs), _vp, ctypes.c_size_t, _vp]
+        L.ssd_prefill_varlen_marked.restype = ctypes.c_int
+        L.ssd_prefill_varlen_marked.argtypes = [ctypes.POINTER(PrefillArgs), _vp, ctypes.c_size_t, _vp, _vp]
         L.ssd_prefill_varlen_noalloc.restype = ctypes.c_int
         L.ssd_prefill_varlen_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
         L.ssm_decode_update.restype = ctypes.c_int
@@ -268,10 +271,12 @@ def ssd_prefill_varlen(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, la
                        out=None, init_slot=None, chunk_slot=None, state_cache=None, D=None,
                        dt_bias=None, z=None, dt_softplus=True, dt_limit=(0.0, math.inf),
                        null_block_id=0, chunk_size=None, workspace=None, err_word=None, stream=None,
-                       seq_order=None, wait_limit_cycles=0):
+                       seq_order=None, wait_limit_cycles=0, mark=None):
     """Varlen SSD prefill on device tensors; returns ``out`` ([T,H,P], x's dtype).
 
-    ``workspace`` (uint8 CUDA tensor) is allocated with torch when omitted.
+    ``workspace`` (uint8 CUDA tensor) is allocated with torch when omitted.  ``mark``: a
+    ``torch.cuda.Event`` the library records right before the call's main kernel
+    (``ssd_prefill_varlen_marked``), for timing the call's kernels apart.
     """
     if out is None:
         out = torch.empty_like(x)
@@ -281,8 +286,14 @@ def ssd_prefill_varlen(x, dt, A, B, C, cu_seqlens, cu_chunk_seqlens, seq_idx, la
     need = ssd_prefill_workspace_size(a)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
-    rc = lib().ssd_prefill_varlen(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
-                                  workspace.numel(), _stream(stream))
+    if mark is None:
+        rc = lib().ssd_prefill_varlen(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
+                                      workspace.numel(), _stream(stream))
+    else:
+        if not mark.cuda_event:  # torch makes its events on their first record
+            mark.record()
+        rc = lib().ssd_prefill_varlen_marked(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()),
+                                             workspace.numel(), _stream(stream), ctypes.c_void_p(mark.cuda_event))
     if rc != SSD_OK:
         raise SSDError("ssd_prefill_varlen", rc)
     return out

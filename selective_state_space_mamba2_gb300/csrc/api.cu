@@ -84,16 +84,17 @@ ssd_status_t check_decode(const ssm_decode_args *a) {
     return SSD_OK;
 }
 
-// The prefill's workspace check and launch; after_prep as for tc_prefill_launch (recorded only
-// on the tensor-core path).
+// The prefill's workspace check and launch.  after_prep and before_fused as for
+// tc_prefill_launch; on the CUDA-core path before_fused is recorded before its first kernel and
+// after_prep not at all.
 ssd_status_t prefill_checked_launch(const ssd_prefill_args *a, void *workspace, size_t workspace_bytes,
-                                    cudaStream_t cs, cudaEvent_t after_prep) {
+                                    cudaStream_t cs, cudaEvent_t after_prep, cudaEvent_t before_fused = nullptr) {
     // bf16 with headdim 64 and dstate 128: the fused tensor-core kernel
     if (ssd::tc_prefill_supported(*a)) {
         if (!workspace || workspace_bytes < ssd::tc_prefill_workspace(*a) ||
             (reinterpret_cast<uintptr_t>(workspace) & 255u))
             return SSD_ERR_WORKSPACE;
-        return from_cuda(ssd::tc_prefill_launch(*a, workspace, cs, after_prep));
+        return from_cuda(ssd::tc_prefill_launch(*a, workspace, cs, after_prep, before_fused));
     }
     if (!ssd::simt_prefill_supported(*a)) return SSD_ERR_UNSUPPORTED;
     const size_t need = ssd::simt_prefill_workspace(*a, nullptr, nullptr);
@@ -101,6 +102,7 @@ ssd_status_t prefill_checked_launch(const ssd_prefill_args *a, void *workspace, 
         return SSD_ERR_WORKSPACE;
     ssd::PrefillWorkspace ws;
     ssd::simt_prefill_workspace(*a, &ws, workspace);
+    if (before_fused && cudaEventRecord(before_fused, cs) != cudaSuccess) return SSD_ERR_CUDA;
     return from_cuda(ssd::simt_prefill_launch(*a, ws, cs));
 }
 
@@ -151,6 +153,14 @@ extern "C" ssd_status_t ssd_prefill_varlen(const ssd_prefill_args *a, void *work
     const ssd_status_t st = check_prefill(a);
     if (st != SSD_OK || a->total_tokens == 0) return st;
     return prefill_checked_launch(a, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" ssd_status_t ssd_prefill_varlen_marked(const ssd_prefill_args *a, void *workspace, size_t workspace_bytes,
+                                                  ssd_stream_t stream, void *event_before_fused) {
+    const ssd_status_t st = check_prefill(a);
+    if (st != SSD_OK || a->total_tokens == 0) return st;
+    return prefill_checked_launch(a, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                                  static_cast<cudaEvent_t>(event_before_fused));
 }
 
 extern "C" ssd_status_t ssm_decode_update(const ssm_decode_args *a, ssd_stream_t stream) {

@@ -89,9 +89,10 @@ bool tc_prefill_supported(const ssd_prefill_args &a);
 int tc_prefill_segments(const ssd_prefill_args &a);
 size_t tc_prefill_workspace(const ssd_prefill_args &a);
 // after_prep: recorded on s once the prep kernel is queued (before the segment pass and the
-// fused kernel), or nullptr
+// fused kernel), or nullptr; before_fused: recorded right before the fused kernel (after the
+// segment pass, if any), or nullptr
 cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s,
-                              cudaEvent_t after_prep = nullptr);
+                              cudaEvent_t after_prep = nullptr, cudaEvent_t before_fused = nullptr);
 
 bool decode_supported(const ssm_decode_args &a);
 cudaError_t decode_launch(const ssm_decode_args &a, cudaStream_t s);

@@ -1044,7 +1044,8 @@ bool tc_prefill_supported(const ssd_prefill_args &a) {
     return a.dtype == SSD_BF16 && a.headdim == kP && a.dstate == kN && a.total_tokens > 0;
 }
 
-cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s, cudaEvent_t after_prep) {
+cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s, cudaEvent_t after_prep,
+                              cudaEvent_t before_fused) {
     CUtensorMap mX, mB, mC, mY;
     const uint64_t T = (uint64_t)a.total_tokens;
     const size_t bc = (size_t)a.total_tokens * a.ngroups * kN * 2;
@@ -1135,6 +1136,10 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
     auto kernel = p.z ? ssd_prefill_tc_kernel<true, false> : ssd_prefill_tc_kernel<false, false>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
+    if (before_fused) {
+        e = cudaEventRecord(before_fused, s);
+        if (e != cudaSuccess) return e;
+    }
     kernel<<<(unsigned)(grid * p.nseg), kThreads, kSmemBytes, s>>>(mX, mB, mC, mY, p);
     return cudaGetLastError();
 }

@@ -117,6 +117,7 @@ def _prefill_args(**over):
 def test_prefill_host_validation(lib, over, code):
     a = _prefill_args(**over)
     assert lib.ssd_prefill_varlen(ctypes.byref(a), None, 0, None) == code
+    assert lib.ssd_prefill_varlen_marked(ctypes.byref(a), None, 0, None, None) == code
     assert lib.ssd_prefill_workspace_size(ctypes.byref(a)) == 0
 
 

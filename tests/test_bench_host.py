@@ -37,6 +37,11 @@ def test_prefill_and_decode_bytes_by_hand():
     # one live request, one token, one column written: a state load and a store (8) and the
     # token's tensors (10)
     assert bench.decode_bytes(1, 1, 1, 1, 1, 1, 1, 2) == 18
+    # the fused kernel's share: all but dt (2), which the prep kernel reads
+    assert bench.fused_bytes(1, 1, 1, 1, 1, 1, 2) == 12
+    # the long batch: 524,288 tokens, 2048 chunks, H=128: 28.05 GB for the call, 0.13 GB of it dt
+    call = bench.prefill_bytes(524288, 2048, 128, 64, 128, 8, 2)
+    assert call == 28051505152 and call - bench.fused_bytes(524288, 2048, 128, 64, 128, 8, 2) == 524288 * 128 * 2
 
 
 def test_peaks_come_from_the_measured_file_when_present():

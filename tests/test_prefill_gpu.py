@@ -318,3 +318,25 @@ def test_one_sequence_split_into_eight_segments():
                          t["cu_chunk_seqlens"], t["seq_idx"], t["last_chunk_indices"], torch.empty_like(case["x"]))
     assert ssd.ssd_prefill_kernel_count(a) == 3
     _run_and_check(case)
+
+
+@pytest.mark.parametrize("P", [64, 32])
+def test_marked_call_records_its_event_and_changes_nothing(P):
+    """ssd_prefill_varlen_marked records the caller's event before the main kernel (after the prep
+    kernel on the tensor-core path, before everything on the CUDA-core path) and gives the bits of
+    the plain call."""
+    case = W.prefill_case(60 + P, [700, 300], [0, 40], 4, P, 128, 2, 256, device=DEV, has_init=[False, True],
+                          num_slots=24)
+    before = case["cache"].clone()
+    y0, meta = PT.run_prefill(case)
+    torch.cuda.synchronize()
+    after = case["cache"].clone()
+    case["cache"].copy_(before)
+    start, mark, end = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    start.record()
+    y1, _ = PT.run_prefill(case, meta=meta, mark=mark)
+    end.record()
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    assert torch.equal(after.view(torch.int32), case["cache"].view(torch.int32))
+    assert start.elapsed_time(mark) >= 0 and mark.elapsed_time(end) > 0
