@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    launch_dependents();  // the fused kernel after the segment pass may be scheduled (small calls)
     const int nsg = kState ? p.nseg - 1 : p.nseg;  // segments with a CTA in this launch
     const int slot_r = blockIdx.x / (p.H * nsg);
     const int jh = blockIdx.x - slot_r * p.H * nsg;
@@ -348,6 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *sTM;
+    // In calls that cut sequences into segments this kernel is a programmatic dependent of the
+    // one before it (the prep kernel, or the segment pass): everything above reads only the
+    // call's arguments, and from here on that kernel's results (the fp16 B and C, delta, the
+    // cumsum, the segment states) must be complete.
+    grid_dependency_wait();
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------ TMA producer ----
@@ -924,6 +930,7 @@ constexpr int kPrepThreads = 128;  // 4 warps
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
     __shared__ float sC[32][129], sD[32][129];  // one block's outputs: 32 heads x 128 tokens (padded)
     __shared__ float sTail[4][32];              // per warp and head: the sum over its 32 tokens
+    launch_dependents();  // the next kernel of a small call may set itself up meanwhile
     // The scan CTAs (the first nscan) compute their piece first.  When there are enough of them
     // (large calls), every CTA then converts its grid-stride share of B and C, so the conversion's
     // bandwidth-bound work runs beside the scan's latency-bound CTAs throughout the grid; small
@@ -1044,6 +1051,27 @@ bool tc_prefill_supported(const ssd_prefill_args &a) {
     return a.dtype == SSD_BF16 && a.headdim == kP && a.dstate == kN && a.total_tokens > 0;
 }
 
+// A launch of the fused kernel (or the segment pass) that may begin while the kernel before it on
+// the stream is finishing: its CTAs set up shared memory and TMEM, then wait in
+// grid_dependency_wait() for that kernel's results.  Used for calls small enough to be cut into
+// segments, where the launch and the prologue are a visible part of the call; the large calls are
+// launched plainly (their CTAs could only wait on SMs the prep kernel still needs).
+using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams);
+cudaError_t launch_tc(TcKernel k, unsigned grid, bool programmatic, cudaStream_t s, const CUtensorMap &mX,
+                      const CUtensorMap &mB, const CUtensorMap &mC, const CUtensorMap &mY, const TcParams &p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, mX, mB, mC, mY, p);
+}
+
 cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaStream_t s, cudaEvent_t after_prep,
                               cudaEvent_t before_fused) {
     CUtensorMap mX, mB, mC, mY;
@@ -1129,8 +1157,8 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
         auto seg_kernel = ssd_prefill_tc_kernel<false, true>;
         e = cudaFuncSetAttribute(seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        seg_kernel<<<(unsigned)(grid * (p.nseg - 1)), kThreads, kSmemBytes, s>>>(mX, mB, mC, mY, p);
-        e = cudaGetLastError();
+        // programmatic unless an event was recorded after the prep kernel (the mixed step's)
+        e = launch_tc(seg_kernel, (unsigned)(grid * (p.nseg - 1)), !after_prep, s, mX, mB, mC, mY, p);
         if (e != cudaSuccess) return e;
     }
     auto kernel = p.z ? ssd_prefill_tc_kernel<true, false> : ssd_prefill_tc_kernel<false, false>;
@@ -1140,8 +1168,9 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
         e = cudaEventRecord(before_fused, s);
         if (e != cudaSuccess) return e;
     }
-    kernel<<<(unsigned)(grid * p.nseg), kThreads, kSmemBytes, s>>>(mX, mB, mC, mY, p);
-    return cudaGetLastError();
+    // programmatic only after the segment pass (small calls), and not when an event is recorded
+    // right before the launch (the caller's mark), or after the prep kernel with no segment pass
+    return launch_tc(kernel, (unsigned)(grid * p.nseg), p.nseg > 1 && !before_fused, s, mX, mB, mC, mY, p);
 }
 
 }  // namespace ssd

@@ -81,6 +81,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
     return true;
 }
 
+// ---------------------------------------------- programmatic launch ----
+// In a kernel launched as a programmatic dependent of the one before it on the stream: wait until
+// that kernel has completed and its writes are visible (a no-op in a kernel launched normally).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let a programmatic dependent of this kernel be scheduled (a no-op without one).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------- packed fp32 ----
 // Two fp32 lanes in one instruction (each rounded as the scalar operation would be).
 __device__ __forceinline__ uint64_t f2_bits(float2 v) { return *reinterpret_cast<uint64_t *>(&v); }
