@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    launch_dependents();  // the fused kernel after the segment pass may be scheduled (small calls)
+    launch_dependents();  // the fused kernel after the segment pass may be scheduled
     const int nsg = kState ? p.nseg - 1 : p.nseg;  // segments with a CTA in this launch
     const int slot_r = blockIdx.x / (p.H * nsg);
     const int jh = blockIdx.x - slot_r * p.H * nsg;
@@ -349,10 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *sTM;
-    // In calls that cut sequences into segments this kernel is a programmatic dependent of the
-    // one before it (the prep kernel, or the segment pass): everything above reads only the
-    // call's arguments, and from here on that kernel's results (the fp16 B and C, delta, the
-    // cumsum, the segment states) must be complete.
+    // This kernel is launched as a programmatic dependent of the one before it (the prep kernel,
+    // or the segment pass): everything above reads only the call's arguments, and from here on
+    // that kernel's results (the fp16 B and C, delta, the cumsum, the segment states) must be
+    // complete.
     grid_dependency_wait();
 
     if (warp == kProducerWarp) {
@@ -930,7 +930,7 @@ constexpr int kPrepThreads = 128;  // 4 warps
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
     __shared__ float sC[32][129], sD[32][129];  // one block's outputs: 32 heads x 128 tokens (padded)
     __shared__ float sTail[4][32];              // per warp and head: the sum over its 32 tokens
-    launch_dependents();  // the next kernel of a small call may set itself up meanwhile
+    launch_dependents();  // the call's next kernel may set itself up meanwhile
     // The scan CTAs (the first nscan) compute their piece first.  When there are enough of them
     // (large calls), every CTA then converts its grid-stride share of B and C, so the conversion's
     // bandwidth-bound work runs beside the scan's latency-bound CTAs throughout the grid; small
@@ -1052,10 +1052,8 @@ bool tc_prefill_supported(const ssd_prefill_args &a) {
 }
 
 // A launch of the fused kernel (or the segment pass) that may begin while the kernel before it on
-// the stream is finishing: its CTAs set up shared memory and TMEM, then wait in
-// grid_dependency_wait() for that kernel's results.  Used for calls small enough to be cut into
-// segments, where the launch and the prologue are a visible part of the call; the large calls are
-// launched plainly (their CTAs could only wait on SMs the prep kernel still needs).
+// the stream is finishing: its CTAs set up shared memory and TMEM as SMs free up, then wait in
+// grid_dependency_wait() for that kernel's results.
 using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams);
 cudaError_t launch_tc(TcKernel k, unsigned grid, bool programmatic, cudaStream_t s, const CUtensorMap &mX,
                       const CUtensorMap &mB, const CUtensorMap &mC, const CUtensorMap &mY, const TcParams &p) {
@@ -1168,9 +1166,10 @@ cudaError_t tc_prefill_launch(const ssd_prefill_args &a, void *workspace, cudaSt
         e = cudaEventRecord(before_fused, s);
         if (e != cudaSuccess) return e;
     }
-    // programmatic only after the segment pass (small calls), and not when an event is recorded
-    // right before the launch (the caller's mark), or after the prep kernel with no segment pass
-    return launch_tc(kernel, (unsigned)(grid * p.nseg), p.nseg > 1 && !before_fused, s, mX, mB, mC, mY, p);
+    // programmatic unless an event sits between it and the kernel before it (the caller's mark,
+    // or the mixed step's event after the prep kernel when there is no segment pass)
+    return launch_tc(kernel, (unsigned)(grid * p.nseg), !before_fused && !(p.nseg == 1 && after_prep), s, mX, mB,
+                     mC, mY, p);
 }
 
 }  // namespace ssd
