@@ -82,12 +82,12 @@ def _sm_max_mhz():
 # ------------------------------------------------------------- byte counts --
 
 # DRAM traffic of one prefill call (tensor-core path, no segment split), from one ncu capture of both
-# its kernels on 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256: prep_kernel 285,269,504 B read +
-# 286,591,488 B written; ssd_prefill_tc_kernel 1,424,121,344 B read + 2,090,929,408 B written.  Scaled by
+# its kernels on 8 x 8192 tokens at H=128, P=64, N=128, G=8, chunk 256: prep_kernel 285,258,752 B read +
+# 286,390,528 B written; ssd_prefill_tc_kernel 1,424,511,488 B read + 2,090,916,864 B written.  Scaled by
 # tokens (x, y, B/C, delta and one state per 256-token chunk all grow with them).  Only for that head
 # configuration and this kernel version; the summary is in profiles/.
-FUSED_TRAFFIC_PER_TOKEN = (1424121344 + 2090929408) / 65536
-PREFILL_TRAFFIC_PER_TOKEN = (285269504 + 286591488) / 65536 + FUSED_TRAFFIC_PER_TOKEN
+FUSED_TRAFFIC_PER_TOKEN = (1424511488 + 2090916864) / 65536
+PREFILL_TRAFFIC_PER_TOKEN = (285258752 + 286390528) / 65536 + FUSED_TRAFFIC_PER_TOKEN
 PREFILL_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of prep_kernel and ssd_prefill_tc_kernel "
                           "on 8 x 8192 tokens, scaled by tokens")
 FUSED_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of ssd_prefill_tc_kernel on 8 x 8192 "
