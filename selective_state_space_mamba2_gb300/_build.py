@@ -39,9 +39,10 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     if (os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(srcp)
             and os.path.getmtime(obj) >= _headers_mtime() and not verbose_ptxas):
         return obj
-    cmd = [nvcc()] + ARCH + NVCC_FLAGS + ["-c", srcp, "-o", obj + ".tmp"]
+    tmp = obj + ".tmp.%d" % os.getpid()  # per process: concurrent builds (one per rank) never share a file
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + ["-c", srcp, "-o", tmp]
     if src.endswith(".cpp"):
-        cmd = [nvcc(), "-x", "c++"] + NVCC_FLAGS + ["-c", srcp, "-o", obj + ".tmp"]
+        cmd = [nvcc(), "-x", "c++"] + NVCC_FLAGS + ["-c", srcp, "-o", tmp]
     elif verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -49,7 +50,7 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
         raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, res.stdout, res.stderr))
     if verbose_ptxas:
         sys.stderr.write(res.stderr)
-    os.replace(obj + ".tmp", obj)
+    os.replace(tmp, obj)
     return obj
 
 
